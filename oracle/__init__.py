@@ -1,0 +1,25 @@
+"""Plain, slow CPU oracle of the MoonEP layer path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this package: only the test-suite, the package smoke check and the
+benchmark's CPU-baseline / reference leg use it.  It shares no code with the
+CUDA library (no headers, helpers, tables or constants) and never reads a value
+the CUDA path produced.
+
+Modules:
+
+* ``planner`` -- histogram, global ordinals, the constructive balancing planner
+  of Theorem 1 with a fixed tie-break, the per-rank expert-grouped buffer layout
+  (``cu_seqlens``) and the destination / inverse permutation of every token
+  copy.
+* ``layer``   -- bf16 rounding, the per-expert GEMM, the gate-weighted combine
+  and ``reduce_grad``.
+* ``theory``  -- the imbalance metric (maxvio), Theorem 2's bound, and a brute
+  force minimum-redundancy search (max-flow feasibility) for tiny inputs.
+
+Parity status: every function above is pinned by tests against facts the
+pages or mathematics fix, except one: *which* copies the planner moves (the
+concrete tie-break) has no external reference, only its invariants do.  That
+choice is "parity unpinned" beyond those invariants.
+"""
+from . import planner, layer, theory  # noqa: F401
