@@ -1,0 +1,193 @@
+/*
+ * moonep.h -- C ABI of the GB300 (sm_103a) MoonEP layer path.
+ *
+ * R expert-parallel ranks are simulated as partitions of one GPU's memory.
+ * One MoE layer runs as six stream-ordered calls:
+ *
+ *   moonep_plan              histogram + constructive balancing plan + per-copy
+ *                            destinations (all on the device, no host sync)
+ *   moonep_prefetch_weights  copy home expert weights into the prefetch slots
+ *   moonep_dispatch          fused permute: every token copy to its final row
+ *   moonep_grouped_gemm      Y = recv x W over the [E+B, H, H'] weight rows
+ *   moonep_combine           fused unpermute, weighted by the top-K gates
+ *   moonep_reduce_grad       fold the slot gradients back into the home rows
+ *
+ * Symbols: R ranks, E experts, L = E/R experts homed on each rank
+ * (home(e) = e / L), B prefetch slots per rank, K experts per token, S tokens
+ * per rank, C = S*K copies per rank, N = R*C copies in all, H the hidden size,
+ * Hp = H' the expert FFN width.
+ *
+ * Conventions for every call
+ *  - Memory: the caller allocates and frees every buffer, including the plan
+ *    workspace.  The library never allocates, frees or synchronises, except
+ *    moonep_read_status and moonep_plan_export, which say so.
+ *  - Pointers are device pointers unless stated; each must be 16-byte aligned
+ *    (MOONEP_ERR_ALIGN otherwise).  bf16 values are passed as their 16-bit
+ *    patterns (uint16_t).  Arrays are dense, row-major, no padding.
+ *  - stream is a cudaStream_t (NULL = legacy default stream).  All work is
+ *    enqueued on it; shapes and launch configurations depend only on the dims,
+ *    never on routing, so a sequence of calls can be captured in a CUDA graph.
+ *  - Return value: a host-detected status (0 = MOONEP_OK), returned before
+ *    anything is enqueued.  Conditions only the device can see (bad routing,
+ *    a device wait that ran out) are OR-ed into a status word inside the plan
+ *    workspace; every later kernel that uses that plan then returns without
+ *    writing anything.  Read it with moonep_read_status.
+ */
+#ifndef MOONEP_H
+#define MOONEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moonep_dims {
+  int32_t R, E, B, K, S, H, Hp;
+  int32_t mode; /* 0 = training (requires B >= E/R), 1 = inference (B >= 0) */
+} moonep_dims;
+
+enum moonep_status {
+  MOONEP_OK = 0,
+  MOONEP_ERR_ARG = 1,      /* null pointer, non-positive dimension, bad mode   */
+  MOONEP_ERR_ALIGN = 2,    /* a pointer is not 16-byte aligned                 */
+  MOONEP_ERR_SLOTS = 3,    /* training mode with B < E/R                       */
+  MOONEP_ERR_SHAPE = 4,    /* E % R != 0, K > E, E > 4096, H or Hp not a multiple
+                              of 64, or N, R*B*H or E*H reaches 2^31            */
+  MOONEP_ERR_CUDA = 5,     /* a CUDA runtime call or launch failed             */
+  /* device-detected bits, OR-ed into the workspace status word */
+  MOONEP_ERR_ROUTING = 0x100,  /* an expert id outside [0,E) or repeated within a token */
+  MOONEP_ERR_INTERNAL = 0x200, /* a planner invariant failed (cannot happen for valid routing) */
+  MOONEP_ERR_TIMEOUT = 0x400   /* a bounded device-side wait gave up           */
+};
+
+/* Byte offsets of the tables inside the plan workspace (all 256-byte aligned).
+ * Integer tables are int32 unless noted. */
+typedef struct moonep_plan_layout {
+  size_t total_bytes;
+  size_t status;       /* int32[1]   sticky device status word                   */
+  size_t counters;     /* int32[8]   n_fills, n_mtiles, n_occupied, n_reduce ... */
+  size_t counts;       /* int32[R][nchunk][E] per-chunk counts, then bases       */
+  size_t T;            /* int32[E]   copies routed to each expert                */
+  size_t load;         /* int32[R]   copies routed to each home rank's experts   */
+  size_t keep;         /* int32[E]   copies of e computed on its home rank       */
+  size_t gidx;         /* int32[R][S][K] ordinal of each copy within its expert  */
+  size_t fills;        /* int32[R-1][3] (u, o, d) in the order performed         */
+  size_t slot_expert;  /* int32[R][B] expert held by slot (u,j), -1 if empty     */
+  size_t n_recv;       /* int32[R]   distinct remote experts rank u computes     */
+  size_t src;          /* int32[R]   the single rank u receives from, -1 if none */
+  size_t cu_seqlens;   /* int32[R][E+B+1] group boundaries of each rank's buffer */
+  size_t dst;          /* int32[R][S][K] destination row u*C + row of each copy  */
+  size_t inverse;      /* int32[R*C] flat copy id (r*S+s)*K+k of each row        */
+  size_t pieces;       /* internal: per-expert ranges of ordinals and their rows */
+  size_t occupied;     /* int32[R*B] occupied slot ids u*B+j, ascending          */
+  size_t reduce;       /* internal: per-expert slot lists for reduce_grad        */
+  size_t mtiles;       /* internal: 128-row GEMM tiles (int32[4] each)           */
+  int32_t nchunk;      /* token chunks per rank used by the histogram            */
+  int32_t max_mtiles;
+} moonep_plan_layout;
+
+/* Index of each counter in the `counters` table. */
+enum moonep_counter {
+  MOONEP_CNT_FILLS = 0,    /* fills performed (<= R-1)                     */
+  MOONEP_CNT_MTILES = 1,   /* 128-row GEMM tiles over all ranks and groups */
+  MOONEP_CNT_OCCUPIED = 2, /* occupied prefetch slots                      */
+  MOONEP_CNT_REDUCE = 3    /* home experts with at least one slot copy     */
+};
+
+/* Size in bytes of the plan workspace for `dims` (host only, no CUDA call).
+ * Returns MOONEP_ERR_* for invalid dims. */
+int moonep_plan_workspace_bytes(const moonep_dims* dims, size_t* bytes);
+
+/* Offsets of the workspace tables, so callers can view them (host only). */
+int moonep_get_plan_layout(const moonep_dims* dims, moonep_plan_layout* out);
+
+/* Plan one layer from the router's top-K output.
+ *
+ * Defines: the histogram, and the constructive balancing plan of Theorem 1
+ * ("Kimi K3 模型结构（8）：训练并行，MoonEP 与四类等待", section 定理 1; "MoonEP :
+ * l'équilibrage parfait", section Le théorème): ranks with fewer than C copies
+ * on their home experts are underloaded, those with more are overloaded; the
+ * smallest-id underloaded rank u is filled to exactly C from the smallest-id
+ * overloaded rank o, taking o's local experts in descending id and, inside an
+ * expert, the copies with the highest ordinal first; o goes back to the set
+ * matching its new load; at most R-1 fills.  Then the buffer layout of the
+ * framework contract ("Moonshot AI 开源 MoonEP", contract paragraph): rank u's
+ * C rows are grouped by weight row g in [0, E+B) ascending (rows [0,E) home
+ * experts, [E, E+B) slots), copies in ascending ordinal inside a group,
+ * cu_seqlens[u][g] the first row of group g; and each copy's destination
+ * ("在线规划、零拷贝、静态 shape": the planner fixes every copy's final position).
+ * In inference mode (mode 1) received experts beyond the B slots use their
+ * home row g = e on the receiving rank.
+ *
+ * topk_idx : int32 [R][S][K] expert ids (device, read only).
+ * plan_ws  : workspace of moonep_plan_workspace_bytes (device, overwritten).
+ * Routing errors set MOONEP_ERR_ROUTING in the workspace status word. */
+int moonep_plan(const moonep_dims* dims, const int32_t* topk_idx, void* plan_ws,
+                void* stream);
+
+/* Fill the prefetch slots: w_slot[u][j] = w_home[slot_expert[u][j]] for every
+ * occupied slot; empty slots are not written ("Moonshot AI 开源 MoonEP": rows
+ * [E, E+B) are local prefetch slots filled by buffer.prefetch_weight).
+ * w_home : bf16 [E][H][Hp] (read).  w_slot : bf16 [R][B][H][Hp] (written). */
+int moonep_prefetch_weights(const moonep_dims* dims, void* plan_ws,
+                            const uint16_t* w_home, uint16_t* w_slot, void* stream);
+
+/* Fused permute: recv[dst[r][s][k]] = x[r][s] for every copy ("Kimi K3
+ * 模型结构（8）", section 在线规划、零拷贝、静态 shape: tokens go straight to their
+ * expert-grouped position in a fixed S*K buffer per rank).
+ * x : bf16 [R][S][H] (read).  recv : bf16 [R][C][H] (every row written). */
+int moonep_dispatch(const moonep_dims* dims, void* plan_ws, const uint16_t* x,
+                    uint16_t* recv, void* stream);
+
+/* Grouped GEMM over the [E+B, H, Hp] weight rows ("Moonshot AI 开源 MoonEP",
+ * contract paragraph: the grouped GEMM addresses experts only by row index,
+ * cu_seqlens chooses the active rows).  For each rank u and group g, rows
+ * cu[u][g]..cu[u][g+1] of recv[u] are multiplied by W(u,g) = w_home[g] if
+ * g < E, else w_slot[u][g-E]; fp32 accumulation, bf16 (round to nearest
+ * even) output.  Tensor cores (tcgen05, TMEM accumulators, TMA-fed).
+ * recv : bf16 [R][C][H].  w_home : bf16 [E][H][Hp].  w_slot : bf16
+ * [R][B][H][Hp] (may be NULL when B == 0).  y : bf16 [R][C][Hp] (written).
+ * Requires H % 64 == 0 and Hp % 64 == 0 (else MOONEP_ERR_SHAPE). */
+int moonep_grouped_gemm(const moonep_dims* dims, void* plan_ws, const uint16_t* recv,
+                        const uint16_t* w_home, const uint16_t* w_slot, uint16_t* y,
+                        void* stream);
+
+/* Fused unpermute/combine: out[r][s] = bf16( sum over k ascending of
+ * gates[r][s][k] * y[dst[r][s][k]] ), fp32 accumulation ("Kimi K3 模型结构（8）",
+ * section 在线规划、零拷贝、静态 shape: every (token, expert) pair carries its own
+ * fp32 router weight, applied to that expert's output at combine).
+ * y : bf16 [R][C][Hp].  gates : fp32 [R][S][K].  out : bf16 [R][S][Hp]. */
+int moonep_combine(const moonep_dims* dims, void* plan_ws, const uint16_t* y,
+                   const float* gates, uint16_t* out, void* stream);
+
+/* reduce_grad ("Moonshot AI 开源 MoonEP", contract paragraph: slot gradients
+ * live in separate reduce buffers seen as one [R, B, H, Hp] view; each home
+ * expert's gradient receives the slots holding it, and consumed slots are
+ * zeroed).  For every expert e with occupied slots (u,j), ascending (u,j):
+ * g_home[e] += g_slot[u][j] in fp32, then g_slot[u][j] = +0.0.  Unoccupied
+ * slots are not touched.
+ * g_home : fp32 [E][H][Hp] (updated).  g_slot : fp32 [R][B][H][Hp] (updated). */
+int moonep_reduce_grad(const moonep_dims* dims, void* plan_ws, float* g_home,
+                       float* g_slot, void* stream);
+
+/* Copy the workspace status word to *host_status.  SYNCHRONISES the stream. */
+int moonep_read_status(const moonep_dims* dims, const void* plan_ws,
+                       int32_t* host_status, void* stream);
+
+/* Copy the whole workspace to host memory (host_dst, total_bytes long), for
+ * tests and debugging.  SYNCHRONISES the stream. */
+int moonep_plan_export(const moonep_dims* dims, const void* plan_ws, void* host_dst,
+                       void* stream);
+
+/* Text for a status code (host or device bits). */
+const char* moonep_status_string(int status);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t moonep_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOONEP_H */

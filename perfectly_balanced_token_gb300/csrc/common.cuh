@@ -1,0 +1,80 @@
+// Internal definitions shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moonep.h"
+
+namespace moonep {
+
+constexpr int kMaxExperts = 4096;   // smem histograms hold E counters per warp
+constexpr int kChunkCopies = 4096;  // copies per histogram chunk (rounded to tokens)
+constexpr int kTileM = 128;         // GEMM rows per tile (one tcgen05 M=128 tile)
+constexpr int kHistWarps = 8;
+
+// Per-expert migrated range of global ordinals [lo, hi) and where it goes.
+struct Piece {
+  int32_t lo, hi, u, g;
+};
+
+// One 128-row GEMM tile: recv/y row of its first row, valid rows, the weight
+// it multiplies (>= 0: home expert id; < 0: -1 - slot id u*B+j) and its rank.
+struct MTile {
+  int32_t row0, rows, wsel, u;
+};
+
+// Device-side view of the workspace, resolved from the layout.
+struct PlanPtrs {
+  int32_t* status;
+  int32_t* counters;
+  int32_t* counts;
+  int32_t* T;
+  int32_t* load;
+  int32_t* keep;
+  int32_t* gidx;
+  int32_t* fills;
+  int32_t* slot_expert;
+  int32_t* n_recv;
+  int32_t* src;
+  int32_t* cu;
+  int32_t* dst;
+  int32_t* inverse;
+  Piece* pieces;        // [E][R]
+  int32_t* piece_n;     // [E]
+  int32_t* piece_base;  // [E][R] row_base = u*C + cu[u][g] - lo
+  int32_t* home_base;   // [E] home rank's row of ordinal 0 of e
+  int32_t* occupied;    // [R*B]
+  int32_t* red_slots;   // [E][R]
+  int32_t* red_n;       // [E]
+  int32_t* red_list;    // [E] experts with >= 1 slot copy
+  int32_t* rank_tiles;  // [R+1] tile offset of each rank
+  MTile* mtiles;        // [max_mtiles]
+};
+
+struct Dims {
+  int R, E, B, K, S, H, Hp, mode;
+  int L, C, N;
+  int nchunk, chunk_tokens, max_mtiles;
+};
+
+// Workspace layout (host computes it; kernels receive resolved pointers).
+struct Layout {
+  moonep_plan_layout pub;
+  size_t pieces, piece_n, piece_base, home_base, red_slots, red_n, red_list, rank_tiles;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_error(int32_t* status, int32_t bit) {
+  atomicOr(status, bit);
+}
+
+__device__ __forceinline__ bool plan_failed(const int32_t* status) {
+  return *reinterpret_cast<const volatile int32_t*>(status) != 0;
+}
+
+}  // namespace moonep

@@ -1,0 +1,423 @@
+// Grouped GEMM over the [E+B, H, H'] weight rows on 5th-generation tensor cores.
+//
+// "Moonshot AI 开源 MoonEP", contract paragraph: one weight tensor [E+B, H, H']
+// per projection, rows [0,E) the home experts of every rank, rows [E, E+B) this
+// rank's prefetch slots; cu_seqlens over the E+B rows selects the active rows.
+// For rank u and group g the rows cu[u][g]..cu[u][g+1] of recv[u] are
+// multiplied by W_home[g] (g < E) or by slot (u, g-E).
+//
+// Design (sm_103a):
+//  * persistent CTAs, one per SM; the work list is the planner's list of
+//    128-row tiles (device memory), times H'/BN column tiles.  Column tiles of
+//    one row tile are adjacent in the order, so concurrently running CTAs share
+//    the A tile and all tiles of one group share the expert's weights in L2.
+//  * warp 0: TMA producer (A box 64x128 K-major, B boxes 64x64 N-major, both
+//    128-byte swizzled) into a STAGES-deep shared-memory ring;
+//    warp 1: TMEM allocation and the single-thread tcgen05.mma issuer
+//    (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM);
+//    warps 2..5: epilogue, tcgen05.ld of the accumulator, bf16 rounding
+//    (nearest even), masked row stores.  The TMEM accumulator is double
+//    buffered so the epilogue of one tile overlaps the main loop of the next.
+//  * every mbarrier wait is bounded by the global timer; on expiry the kernel
+//    records MOONEP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+//    returns.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moonep {
+
+constexpr int kBK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;     // K of one tcgen05.mma for 16-bit inputs
+constexpr int kGemmThreads = 192;
+constexpr uint64_t kWaitNs = 4000000000ull;  // 4 s per barrier wait
+
+template <int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int kABytes = kTileM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
+};
+
+// -- PTX wrappers -------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.  Gives up when the
+// abort flag is raised by another role or after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+  uint32_t out;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(__uint_as_float(hi_f32)),
+      "f"(__uint_as_float(lo_f32)));
+  return out;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
+// start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
+// byte offset >> 4 in 32-45, descriptor version 1 at bit 46, swizzle mode 2
+// (128 B) in bits 61-63.  Tiles are 1024-byte aligned so the base offset is 0.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
+// bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major (bit 16 =
+// 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
+        const __grid_constant__ CUtensorMap tm_ws, Dims d, PlanPtrs p, uint16_t* __restrict__ y) {
+  using Cfg = GemmCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
+  const int NT = d.Hp / BN;
+  const int total = p.counters[MOONEP_CNT_MTILES] * NT;
+  const int KB = d.H / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_wh);
+    prefetch_tmap(&tm_ws);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const MTile mt = p.mtiles[t / NT];
+        const int n0 = (t % NT) * BN;
+        const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
+        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * d.H;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(full(stage), Cfg::kStageBytes);
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        // wait (time-bounded) for the copies this thread started
+        for (int i = 0; i < min(issued, STAGES); ++i) {
+          if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+          mbar_wait(full(stage), phase, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kTileM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
+            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            umma_bf16(dtm, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit(empty(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        umma_commit(drain);  // completes once every MMA issued so far is done
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lanes 32q..32q+31 are this warp's rows
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const MTile mt = p.mtiles[t / NT];
+      const int n0 = (t % NT) * BN;
+      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int row = q * 32 + lane;
+      const bool valid = row < mt.rows;
+      uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tbase + c * 32, r);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+            o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+            o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+            o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// -- host side ------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* sym = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)sym;
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [outer][inner], box [box_outer][64], 128-byte swizzle.
+static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+static cudaError_t launch_ggemm_cfg(const Dims& d, const PlanPtrs& p, const CUtensorMap& a,
+                                    const CUtensorMap& wh, const CUtensorMap& ws, uint16_t* y,
+                                    int grid, cudaStream_t st) {
+  using Cfg = GemmCfg<BN, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_ggemm<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_ggemm<BN, STAGES><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, p, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* recv,
+                                const void* w_home, const void* w_slot, void* y, cudaStream_t st,
+                                int* launches) {
+  CUtensorMap ta, twh, tws;
+  if (!encode_2d(&ta, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, kTileM)) return cudaErrorInvalidValue;
+  if (!encode_2d(&twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64)) return cudaErrorInvalidValue;
+  const void* ws = (w_slot != nullptr && d.B > 0) ? w_slot : w_home;
+  const uint64_t ws_rows = (w_slot != nullptr && d.B > 0) ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H;
+  if (!encode_2d(&tws, ws, (uint64_t)d.Hp, ws_rows, 64)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int bn = (d.Hp % 256 == 0) ? 256 : (d.Hp % 128 == 0 ? 128 : 64);
+  const long long max_tiles = (long long)d.max_mtiles * (d.Hp / bn);
+  const int grid = (int)std::min<long long>(sms, std::max<long long>(1, max_tiles));
+  cudaError_t e;
+  if (bn == 256) e = launch_ggemm_cfg<256, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else if (bn == 128) e = launch_ggemm_cfg<128, 6>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else e = launch_ggemm_cfg<64, 8>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  if (e == cudaSuccess) *launches += 1;
+  return e;
+}
+
+}  // namespace moonep

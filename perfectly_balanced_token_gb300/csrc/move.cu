@@ -1,0 +1,250 @@
+// Memory-bound kernels of the layer path: weight prefetch into slots, fused
+// permute (dispatch), fused unpermute/combine and reduce_grad.
+//
+// All four move 16-byte vectors with streaming cache hints; each thread issues
+// all of its loads before any dependent store so enough bytes are in flight to
+// keep HBM busy.  Work that depends on the plan (occupied slots, experts with
+// slot gradients) is read from the device-side plan; the grids are fixed by
+// the dims so no host synchronisation is needed.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moonep {
+
+// ---------------------------------------------------------------------------
+// prefetch: w_slot[s] = w_home[slot_expert[s]] for every occupied slot s
+// ("Moonshot AI 开源 MoonEP", contract paragraph: rows [E, E+B) are local prefetch
+// slots filled before the expert GEMM)
+// ---------------------------------------------------------------------------
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVec = 8;                                   // uint4 per thread per item
+constexpr int kCopyChunk = kCopyThreads * kCopyVec * 16;      // 32 KiB per work item
+
+__global__ void __launch_bounds__(kCopyThreads)
+k_prefetch(Dims d, PlanPtrs p, const uint4* __restrict__ w_home, uint4* __restrict__ w_slot) {
+  if (plan_failed(p.status)) return;
+  const size_t vec_per_w = (size_t)d.H * d.Hp * 2 / 16;
+  const int nch = (int)((vec_per_w * 16 + kCopyChunk - 1) / kCopyChunk);
+  const int items = p.counters[MOONEP_CNT_OCCUPIED] * nch;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int s = p.occupied[it / nch];
+    const int e = p.slot_expert[s];
+    const size_t v0 = (size_t)(it % nch) * (kCopyChunk / 16);
+    const uint4* src = w_home + (size_t)e * vec_per_w;
+    uint4* dst = w_slot + (size_t)s * vec_per_w;
+    uint4 v[kCopyVec];
+#pragma unroll
+    for (int i = 0; i < kCopyVec; ++i) {
+      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+      if (a < vec_per_w) v[i] = __ldcs(src + a);
+    }
+#pragma unroll
+    for (int i = 0; i < kCopyVec; ++i) {
+      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+      if (a < vec_per_w) __stcs(dst + a, v[i]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch: recv[dst[r,s,k]] = x[r,s] -- one token row is read once and
+// written K times ("Kimi K3 模型结构（8）", section 在线规划、零拷贝、静态 shape)
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 128;
+
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads)
+k_dispatch(Dims d, PlanPtrs p, const uint4* __restrict__ x, uint4* __restrict__ recv) {
+  if (plan_failed(p.status)) return;
+  const int hv = d.H / 8;  // uint4 per row
+  const int ntok = d.R * d.S;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    const uint4* xr = x + (size_t)t * hv;
+    uint4 v[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int a = threadIdx.x + i * kRowThreads;
+      if (a < hv) v[i] = __ldcs(xr + a);
+    }
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    for (int k = 0; k < d.K; ++k) {
+      uint4* out = recv + (size_t)__ldg(dt + k) * hv;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int a = threadIdx.x + i * kRowThreads;
+        if (a < hv) __stcs(out + a, v[i]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: out[r,s] = bf16( sum_k gates[r,s,k] * y[dst[r,s,k]] ), k ascending,
+// fp32 fused multiply-add ("Kimi K3 模型结构（8）", same section: each expert
+// output is scaled by its own fp32 router weight)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void fma_bf16x8(float* acc, float g, const uint4& v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+  }
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kRowThreads)
+k_combine(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restrict__ gates,
+          uint4* __restrict__ out) {
+  if (plan_failed(p.status)) return;
+  const int hv = d.Hp / 8;
+  const int ntok = d.R * d.S;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    const float* gt = gates + (size_t)t * d.K;
+    for (int a = threadIdx.x; a < hv; a += kRowThreads) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int k0 = 0; k0 < d.K; k0 += KC) {
+        uint4 v[KC];
+        float g[KC];
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          if (k0 + k < d.K) {
+            v[k] = __ldcs(y + (size_t)__ldg(dt + k0 + k) * hv + a);
+            g[k] = __ldg(gt + k0 + k);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+          if (k0 + k < d.K) fma_bf16x8(acc, g[k], v[k]);
+      }
+      uint4 o;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      __stcs(out + (size_t)t * hv + a, o);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// reduce_grad: g_home[e] += g_slot[s] for the slots s holding e (ascending),
+// then g_slot[s] = 0 ("Moonshot AI 开源 MoonEP", contract paragraph)
+// ---------------------------------------------------------------------------
+constexpr int kRedVec = 4;                                 // float4 per thread per item
+constexpr int kRedChunk = kCopyThreads * kRedVec;          // float4 per work item
+
+__global__ void __launch_bounds__(kCopyThreads)
+k_reduce(Dims d, PlanPtrs p, float4* __restrict__ g_home, float4* __restrict__ g_slot) {
+  if (plan_failed(p.status)) return;
+  const size_t v_per = (size_t)d.H * d.Hp / 4;
+  const int nch = (int)((v_per + kRedChunk - 1) / kRedChunk);
+  const int items = p.counters[MOONEP_CNT_REDUCE] * nch;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int e = p.red_list[it / nch];
+    const int n = p.red_n[e];
+    const int32_t* slots = p.red_slots + (size_t)e * d.R;
+    const size_t v0 = (size_t)(it % nch) * kRedChunk;
+    float4* home = g_home + (size_t)e * v_per;
+    float4 acc[kRedVec];
+#pragma unroll
+    for (int i = 0; i < kRedVec; ++i) {
+      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+      if (a < v_per) acc[i] = __ldcs(home + a);
+    }
+    for (int j = 0; j < n; ++j) {
+      float4* sl = g_slot + (size_t)slots[j] * v_per;
+      float4 v[kRedVec];
+#pragma unroll
+      for (int i = 0; i < kRedVec; ++i) {
+        const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+        if (a < v_per) v[i] = __ldcs(sl + a);
+      }
+#pragma unroll
+      for (int i = 0; i < kRedVec; ++i) {
+        const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+        if (a < v_per) {
+          acc[i].x = acc[i].x + v[i].x;
+          acc[i].y = acc[i].y + v[i].y;
+          acc[i].z = acc[i].z + v[i].z;
+          acc[i].w = acc[i].w + v[i].w;
+          __stcs(sl + a, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kRedVec; ++i) {
+      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+      if (a < v_per) __stcs(home + a, acc[i]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+cudaError_t launch_prefetch(const Dims& d, const PlanPtrs& p, const void* w_home, void* w_slot,
+                            cudaStream_t st, int* launches) {
+  if (d.B == 0) return cudaSuccess;
+  const int grid = sm_count() * 8;
+  k_prefetch<<<grid, kCopyThreads, 0, st>>>(d, p, (const uint4*)w_home, (uint4*)w_slot);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const Dims& d, const PlanPtrs& p, const void* x, void* recv,
+                            cudaStream_t st, int* launches) {
+  const int hv = d.H / 8;
+  const int vpt = (hv + kRowThreads - 1) / kRowThreads;
+  const int ntok = d.R * d.S;
+  const int grid = min(ntok, sm_count() * 16);
+  const uint4* xs = (const uint4*)x;
+  uint4* rv = (uint4*)recv;
+  if (vpt <= 1) k_dispatch<1><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
+  else if (vpt <= 2) k_dispatch<2><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
+  else if (vpt <= 4) k_dispatch<4><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
+  else if (vpt <= 8) k_dispatch<8><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
+  else if (vpt <= 16) k_dispatch<16><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
+  else return cudaErrorInvalidValue;
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Dims& d, const PlanPtrs& p, const void* y, const float* gates,
+                           void* out, cudaStream_t st, int* launches) {
+  const int ntok = d.R * d.S;
+  const int grid = min(ntok, sm_count() * 16);
+  if (d.K >= 8)
+    k_combine<8><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)y, gates, (uint4*)out);
+  else
+    k_combine<4><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)y, gates, (uint4*)out);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const Dims& d, const PlanPtrs& p, float* g_home, float* g_slot,
+                          cudaStream_t st, int* launches) {
+  if (d.B == 0) return cudaSuccess;
+  const int grid = sm_count() * 8;
+  k_reduce<<<grid, kCopyThreads, 0, st>>>(d, p, (float4*)g_home, (float4*)g_slot);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace moonep

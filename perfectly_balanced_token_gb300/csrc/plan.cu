@@ -1,0 +1,385 @@
+// Planner kernels: histogram + stable ordinals, the constructive balancing
+// plan, per-rank buffer tables and per-copy destinations.
+//
+// The construction follows Theorem 1 of "Kimi K3 模型结构（8）：训练并行，MoonEP
+// 与四类等待" (section 定理 1) and "MoonEP : l'équilibrage parfait" (section Le
+// théorème): fill one underloaded rank u to exactly C = S*K from one
+// overloaded rank o, put o back in the matching set, repeat; each rank is
+// filled at most once, so its remote copies come from one rank and touch at
+// most E/R experts.  The fixed tie-break: smallest-id u and o; o's experts in
+// descending id; inside an expert the highest global ordinals first.
+//
+// Everything stays on the device: the histogram, plan and tables are produced
+// by four launches whose shapes depend only on the dims ("Kimi K3 模型结构（8）",
+// section 在线规划、零拷贝、静态 shape: static shapes remove the per-layer host
+// synchronisation).
+#include "common.cuh"
+
+namespace moonep {
+
+// ---------------------------------------------------------------------------
+// 1. per-chunk histogram and chunk-local stable ordinals
+//    grid (nchunk, R), kHistWarps warps, smem [kHistWarps][E] counters
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kHistWarps * 32)
+k_hist(Dims d, const int32_t* __restrict__ idx, PlanPtrs p) {
+  extern __shared__ int32_t sh[];
+  const int r = blockIdx.y, chunk = blockIdx.x;
+  const int t0 = chunk * d.chunk_tokens;
+  const int t1 = min(d.S, t0 + d.chunk_tokens);
+  const int ncopy = (t1 - t0) * d.K;
+  const size_t first = ((size_t)r * d.S + t0) * d.K;
+  const int32_t* ids = idx + first;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i < kHistWarps * d.E; i += blockDim.x) sh[i] = 0;
+
+  // validate: ids in range and distinct within each token
+  int bad = 0;
+  for (int t = threadIdx.x; t < t1 - t0; t += blockDim.x) {
+    const int32_t* tok = ids + (size_t)t * d.K;
+    for (int a = 0; a < d.K; ++a) {
+      const int ea = tok[a];
+      bad |= (ea < 0) | (ea >= d.E);
+      for (int b = a + 1; b < d.K; ++b) bad |= (tok[b] == ea);
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) set_error(p.status, MOONEP_ERR_ROUTING);
+    return;
+  }
+
+  // each warp owns a contiguous, 32-aligned sub-range of the chunk's copies
+  const int per = ((ncopy + kHistWarps * 32 - 1) / (kHistWarps * 32)) * 32;
+  const int w_lo = min(ncopy, warp * per), w_hi = min(ncopy, w_lo + per);
+  int32_t* mine = sh + warp * d.E;
+  for (int i = w_lo + lane; i < w_hi; i += 32) atomicAdd(&mine[ids[i]], 1);
+  __syncthreads();
+
+  // exclusive scan across warps per expert -> chunk totals
+  int32_t* cnt = p.counts + ((size_t)r * d.nchunk + chunk) * d.E;
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kHistWarps; ++w) {
+      const int v = sh[w * d.E + e];
+      sh[w * d.E + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+
+  // stable ordinals: 32 copies at a time in order, equal ids ranked by lane
+  int32_t* out = p.gidx + first;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+    const int i = i0 + lane;
+    const bool valid = i < w_hi;
+    const int e = valid ? ids[i] : d.E + lane;  // unique filler never matches
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int before = __popc(peers & lt);
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (valid) base = mine[e];
+    __syncwarp();
+    if (valid && lane == leader) mine[e] = base + __popc(peers);
+    __syncwarp();
+    if (valid) out[i] = base + before;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. single-CTA planner: chunk bases, loads, the fills, slots and row counts
+// ---------------------------------------------------------------------------
+enum : int32_t { kBalanced = 0, kUnder = 1, kOver = 2 };
+
+__global__ void __launch_bounds__(1024)
+k_plan(Dims d, PlanPtrs p) {
+  extern __shared__ int32_t sh[];
+  int32_t* sT = sh;                 // [E]
+  int32_t* sMig = sT + d.E;         // [E]
+  int32_t* sLoad = sMig + d.E;      // [R]
+  int32_t* sState = sLoad + d.R;    // [R]
+  int32_t* sCur = sState + d.R;     // [R]
+  int32_t* sTiles = sCur + d.R;     // [R]
+  if (plan_failed(p.status)) return;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int EB = d.E + d.B;
+
+  // chunk bases (ascending (rank, chunk) == ascending (rank, token)) and T
+  const int rc = d.R * d.nchunk;
+  for (int e = tid; e < d.E; e += nt) {
+    int run = 0;
+    int32_t* c = p.counts + e;
+    for (int i = 0; i < rc; ++i) {
+      const int v = c[(size_t)i * d.E];
+      c[(size_t)i * d.E] = run;
+      run += v;
+    }
+    sT[e] = run;
+    p.T[e] = run;
+    sMig[e] = 0;
+    p.piece_n[e] = 0;
+    p.red_n[e] = 0;
+  }
+  for (int s = tid; s < d.R * d.B; s += nt) p.slot_expert[s] = -1;
+  for (int i = tid; i < d.R * (EB + 1); i += nt) p.cu[i] = 0;
+  for (int h = tid; h < d.R; h += nt) {
+    p.n_recv[h] = 0;
+    p.src[h] = -1;
+    sTiles[h] = 0;
+  }
+  for (int i = tid; i < 3 * max(d.R - 1, 1); i += nt) p.fills[i] = -1;
+  __syncthreads();
+  for (int h = tid; h < d.R; h += nt) {
+    int s = 0;
+    for (int e = h * d.L; e < (h + 1) * d.L; ++e) s += sT[e];
+    sLoad[h] = s;
+    p.load[h] = s;
+    sState[h] = s < d.C ? kUnder : (s > d.C ? kOver : kBalanced);
+    sCur[h] = (h + 1) * d.L - 1;
+  }
+  __syncthreads();
+
+  // the fills, sequential by construction (at most R-1 of them)
+  if (tid == 0) {
+    int nfill = 0;
+    bool ok = true;
+    while (ok) {
+      int u = -1, o = -1;
+      for (int h = 0; h < d.R && (u < 0 || o < 0); ++h) {
+        if (u < 0 && sState[h] == kUnder) u = h;
+        if (o < 0 && sState[h] == kOver) o = h;
+      }
+      if (u < 0) break;
+      if (o < 0 || nfill >= d.R - 1) { ok = false; break; }
+      const int dcopies = d.C - sLoad[u];
+      int need = dcopies, j = 0;
+      while (need > 0) {
+        const int e = sCur[o];
+        if (e < o * d.L) { ok = false; break; }
+        const int left = sT[e] - sMig[e];
+        if (left == 0) { sCur[o] = e - 1; continue; }
+        const int t = min(left, need);
+        const int g = (j < d.B) ? d.E + j : e;  // slot, or inference overflow row
+        if (j < d.B) p.slot_expert[u * d.B + j] = e;
+        const int pi = p.piece_n[e];
+        if (pi >= d.R) { ok = false; break; }
+        p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
+        p.piece_n[e] = pi + 1;
+        p.cu[(size_t)u * (EB + 1) + g + 1] = t;
+        sTiles[u] += (t + kTileM - 1) / kTileM;
+        sMig[e] += t;
+        need -= t;
+        ++j;
+      }
+      if (!ok) break;
+      if (d.mode == 0 && j > d.B) { ok = false; break; }
+      p.fills[3 * nfill + 0] = u;
+      p.fills[3 * nfill + 1] = o;
+      p.fills[3 * nfill + 2] = dcopies;
+      p.n_recv[u] = j;
+      p.src[u] = o;
+      ++nfill;
+      sLoad[u] = d.C;
+      sState[u] = kBalanced;
+      sLoad[o] -= dcopies;
+      sState[o] = sLoad[o] < d.C ? kUnder : (sLoad[o] > d.C ? kOver : kBalanced);
+    }
+    if (!ok) set_error(p.status, MOONEP_ERR_INTERNAL);
+    p.counters[MOONEP_CNT_FILLS] = nfill;
+  }
+  __syncthreads();
+  if (plan_failed(p.status)) return;
+
+  // keep, home rows, per-rank tile counts
+  for (int e = tid; e < d.E; e += nt) {
+    const int k = sT[e] - sMig[e];
+    p.keep[e] = k;
+    const int h = e / d.L;
+    p.cu[(size_t)h * (EB + 1) + e + 1] = k;
+    atomicAdd(&sTiles[h], (k + kTileM - 1) / kTileM);
+  }
+  // reduce lists: the slots holding e in ascending (u, j)
+  for (int s = tid; s < d.R * d.B; s += nt) {
+    const int e = p.slot_expert[s];
+    if (e >= 0) {
+      const int at = atomicAdd(&p.red_n[e], 1);
+      p.red_slots[(size_t)e * d.R + at] = s;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < d.E; e += nt) {
+    const int n = p.red_n[e];
+    int32_t* l = p.red_slots + (size_t)e * d.R;
+    for (int a = 1; a < n; ++a) {  // insertion sort, n <= R-1
+      const int v = l[a];
+      int b = a - 1;
+      while (b >= 0 && l[b] > v) { l[b + 1] = l[b]; --b; }
+      l[b + 1] = v;
+    }
+  }
+  // compact lists (warp 0, ballot prefix keeps ascending order)
+  if (tid < 32) {
+    int n_occ = 0, n_red = 0;
+    for (int s0 = 0; s0 < d.R * d.B; s0 += 32) {
+      const int s = s0 + tid;
+      const bool occ = s < d.R * d.B && p.slot_expert[s] >= 0;
+      const unsigned m = __ballot_sync(0xffffffffu, occ);
+      if (occ) p.occupied[n_occ + __popc(m & ((1u << tid) - 1u))] = s;
+      n_occ += __popc(m);
+    }
+    for (int e0 = 0; e0 < d.E; e0 += 32) {
+      const int e = e0 + tid;
+      const bool has = e < d.E && p.red_n[e] > 0;
+      const unsigned m = __ballot_sync(0xffffffffu, has);
+      if (has) p.red_list[n_red + __popc(m & ((1u << tid) - 1u))] = e;
+      n_red += __popc(m);
+    }
+    if (tid == 0) {
+      p.counters[MOONEP_CNT_OCCUPIED] = n_occ;
+      p.counters[MOONEP_CNT_REDUCE] = n_red;
+      int run = 0;
+      for (int h = 0; h < d.R; ++h) {
+        p.rank_tiles[h] = run;
+        run += sTiles[h];
+      }
+      p.rank_tiles[d.R] = run;
+      p.counters[MOONEP_CNT_MTILES] = run;
+      if (run > d.max_mtiles) set_error(p.status, MOONEP_ERR_INTERNAL);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. per-rank tables: cu_seqlens scan, GEMM tile list, row bases
+//    grid R, 1024 threads
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ void block_scan2(int& a, int& b, int* sa, int* sb) {
+  // inclusive block scan of two ints; sa/sb hold NT/32 partials each
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, a, o);
+    const int yb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) { a += ya; b += yb; }
+  }
+  if (lane == 31) { sa[warp] = a; sb[warp] = b; }
+  __syncthreads();
+  if (warp == 0) {
+    int xa = lane < NT / 32 ? sa[lane] : 0, xb = lane < NT / 32 ? sb[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, xa, o);
+      const int yb = __shfl_up_sync(0xffffffffu, xb, o);
+      if (lane >= o) { xa += ya; xb += yb; }
+    }
+    if (lane < NT / 32) { sa[lane] = xa; sb[lane] = xb; }
+  }
+  __syncthreads();
+  if (warp > 0) { a += sa[warp - 1]; b += sb[warp - 1]; }
+}
+
+__global__ void __launch_bounds__(1024)
+k_tables(Dims d, PlanPtrs p) {
+  __shared__ int sa[32], sb[32];
+  if (plan_failed(p.status)) return;
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int EB = d.E + d.B;
+  int32_t* cu = p.cu + (size_t)u * (EB + 1);
+  // each thread scans a contiguous run of groups
+  const int per = (EB + 1023) / 1024;
+  const int g0 = min(EB, tid * per), g1 = min(EB, g0 + per);
+  int rows_local[8];
+  int rsum = 0, tsum = 0;
+  for (int g = g0, i = 0; g < g1; ++g, ++i) {
+    const int rows = cu[g + 1];
+    if (i < 8) rows_local[i] = rows;
+    rsum += rows;
+    tsum += (rows + kTileM - 1) / kTileM;
+  }
+  int ra = rsum, tb = tsum;
+  block_scan2<1024>(ra, tb, sa, sb);
+  int row = ra - rsum, tile = tb - tsum + p.rank_tiles[u];
+  __syncthreads();  // every thread has read its rows before they are replaced
+  for (int g = g0, i = 0; g < g1; ++g, ++i) {
+    const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 5 for E <= 4096
+    cu[g] = row;
+    const int wsel = (g < d.E) ? g : -1 - (u * d.B + (g - d.E));
+    for (int m = 0; m * kTileM < rows; ++m) {
+      p.mtiles[tile++] = MTile{u * d.C + row + m * kTileM, min(kTileM, rows - m * kTileM), wsel, u};
+    }
+    row += rows;
+  }
+  if (tid == 1023) cu[EB] = row;
+  __syncthreads();
+  // row bases: home experts of u, and every piece that lands on u
+  for (int e = u * d.L + tid; e < (u + 1) * d.L; e += 1024) p.home_base[e] = u * d.C + cu[e];
+  for (int e = tid; e < d.E; e += 1024) {
+    const int n = p.piece_n[e];
+    for (int i = 0; i < n; ++i) {
+      const Piece pc = p.pieces[(size_t)e * d.R + i];
+      if (pc.u == u) p.piece_base[(size_t)e * d.R + i] = u * d.C + cu[pc.g] - pc.lo;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4. destinations and inverse: grid (nchunk, R), 256 threads
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+k_dst(Dims d, const int32_t* __restrict__ idx, PlanPtrs p) {
+  if (plan_failed(p.status)) return;
+  const int r = blockIdx.y, chunk = blockIdx.x;
+  const int t0 = chunk * d.chunk_tokens;
+  const int t1 = min(d.S, t0 + d.chunk_tokens);
+  const int ncopy = (t1 - t0) * d.K;
+  const size_t first = ((size_t)r * d.S + t0) * d.K;
+  const int32_t* base = p.counts + ((size_t)r * d.nchunk + chunk) * d.E;
+  for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
+    const size_t c = first + i;
+    const int e = idx[c];
+    const int q = base[e] + p.gidx[c];
+    p.gidx[c] = q;
+    int row;
+    if (q < p.keep[e]) {
+      row = p.home_base[e] + q;
+    } else {
+      row = -1;
+      const int n = p.piece_n[e];
+      for (int j = 0; j < n; ++j) {
+        const Piece pc = p.pieces[(size_t)e * d.R + j];
+        if (pc.lo <= q && q < pc.hi) { row = p.piece_base[(size_t)e * d.R + j] + q; break; }
+      }
+      if (row < 0) { set_error(p.status, MOONEP_ERR_INTERNAL); continue; }
+    }
+    if (row < 0 || row >= d.N) { set_error(p.status, MOONEP_ERR_INTERNAL); continue; }
+    p.dst[c] = row;
+    p.inverse[row] = (int32_t)c;
+  }
+}
+
+cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cudaStream_t st,
+                        int* launches) {
+  cudaError_t err = cudaMemsetAsync(p.status, 0, 256, st);  // status + counters header
+  if (err != cudaSuccess) return err;
+  const size_t hist_smem = sizeof(int32_t) * kHistWarps * d.E;
+  if (hist_smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(k_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_smem);
+    if (err != cudaSuccess) return err;
+  }
+  k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
+  const size_t plan_smem = sizeof(int32_t) * (2 * d.E + 4 * d.R);
+  if (plan_smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
+    if (err != cudaSuccess) return err;
+  }
+  k_plan<<<1, 1024, plan_smem, st>>>(d, p);
+  k_tables<<<d.R, 1024, 0, st>>>(d, p);
+  k_dst<<<dim3(d.nchunk, d.R), 256, 0, st>>>(d, idx, p);
+  *launches += 4;
+  return cudaGetLastError();
+}
+
+}  // namespace moonep

@@ -1,0 +1,115 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+and rejects bad arguments before enqueueing anything (no GPU needed).
+
+Every call below fails host-side validation, so none of them reaches a CUDA
+launch even on a machine with a GPU; the launch counter proves it.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import perfectly_balanced_token_gb300 as mx
+from perfectly_balanced_token_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "moonep.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from perfectly_balanced_token_gb300.build import build
+    build()
+    return mx.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moonep_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) == 12, names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_dims_validation():
+    good = mx.dims(8, 384, 48, 8, 8192, 7168, 2048)
+    assert mx.moonep_plan_workspace_bytes(good) > 0
+    cases = {
+        _lib.ERR_SLOTS: mx.dims(8, 384, 47, 8, 8192, 7168, 2048, 0),
+        _lib.ERR_SHAPE: mx.dims(8, 380, 48, 8, 8192, 7168, 2048),
+        _lib.ERR_ARG: mx.dims(8, 384, 48, 8, 8192, 7168, 2048, 2),
+    }
+    for code, d in cases.items():
+        with pytest.raises(mx.MoonepError) as ei:
+            mx.moonep_plan_workspace_bytes(d)
+        assert ei.value.status == code
+    shape_bad = [mx.dims(8, 384, 48, 385, 8192, 7168, 2048),   # K > E
+                 mx.dims(8, 384, 48, 8, 8192, 7100, 2048),     # H % 64
+                 mx.dims(8, 384, 48, 8, 8192, 7168, 2000),     # Hp % 64
+                 mx.dims(2, 8192, 4096, 8, 16, 64, 64),        # E > 4096
+                 mx.dims(8, 64, 65, 4, 16, 64, 64, 1),         # B > E
+                 mx.dims(8, 64, 8, 64, 1 << 23, 64, 64)]       # N >= 2^31
+    for d in shape_bad:
+        with pytest.raises(mx.MoonepError) as ei:
+            mx.moonep_plan_workspace_bytes(d)
+        assert ei.value.status == _lib.ERR_SHAPE
+    for d in [mx.dims(0, 8, 2, 2, 16, 64, 64), mx.dims(4, 8, -1, 2, 16, 64, 64, 1)]:
+        with pytest.raises(mx.MoonepError) as ei:
+            mx.moonep_plan_workspace_bytes(d)
+        assert ei.value.status == _lib.ERR_ARG
+    # inference mode accepts B < E/R, including B = 0
+    assert mx.moonep_plan_workspace_bytes(mx.dims(8, 384, 0, 8, 8192, 7168, 2048, 1)) > 0
+
+
+def test_layout_tables_are_aligned_and_inside():
+    d = mx.dims(64, 896, 14, 16, 1024, 4096, 1024)
+    lay = mx.moonep_get_plan_layout(d)
+    offs = [getattr(lay, f) for f in _lib._LAYOUT_FIELDS[1:]]
+    assert lay.counters == 64 and lay.status == 0
+    for o in offs[2:]:
+        assert o % 256 == 0 and o < lay.total_bytes
+    assert lay.nchunk == 4 and lay.max_mtiles >= d.N // 128
+
+
+def test_bad_pointers_rejected_before_launch(lib):
+    n0 = mx.moonep_launch_count()
+    d = mx.dims(4, 8, 2, 2, 16, 64, 128)
+    D = ctypes.byref(d)
+    P = ctypes.c_void_p
+    ws, ok, odd = P(0x10000), P(0x20000), P(0x20004)
+    assert lib.moonep_plan(D, None, ws, None) == _lib.ERR_ARG
+    assert lib.moonep_plan(D, odd, ws, None) == _lib.ERR_ALIGN
+    assert lib.moonep_plan(D, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_plan(D, ok, P(0x10008), None) == _lib.ERR_ALIGN
+    assert lib.moonep_dispatch(D, ws, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_dispatch(D, ws, odd, ok, None) == _lib.ERR_ALIGN
+    assert lib.moonep_prefetch_weights(D, ws, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_grouped_gemm(D, ws, ok, ok, None, ok, None) == _lib.ERR_ARG
+    assert lib.moonep_grouped_gemm(D, ws, ok, odd, ok, ok, None) == _lib.ERR_ALIGN
+    assert lib.moonep_combine(D, ws, ok, None, ok, None) == _lib.ERR_ARG
+    assert lib.moonep_reduce_grad(D, ws, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_read_status(D, ws, None, None) == _lib.ERR_ARG
+    assert lib.moonep_plan_export(D, ws, None, None) == _lib.ERR_ARG
+    bad = mx.dims(4, 8, 1, 2, 16, 64, 128, 0)
+    assert lib.moonep_plan(ctypes.byref(bad), ok, ws, None) == _lib.ERR_SLOTS
+    assert lib.moonep_plan(None, ok, ws, None) == _lib.ERR_ARG
+    assert mx.moonep_launch_count() == n0
+
+
+def test_status_strings():
+    for code in (0, 1, 2, 3, 4, 5, 0x100, 0x200, 0x400, 0x300):
+        s = mx.status_string(code)
+        assert s and s != "unknown status"
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    d = mx.dims(4, 8, 2, 2, 16, 64, 128)
+    with pytest.raises(ValueError):
+        mx.moonep_plan(d, torch.zeros(4 * 16 * 2, dtype=torch.int32),
+                       torch.zeros(mx.moonep_plan_workspace_bytes(d), dtype=torch.uint8))

@@ -1,0 +1,181 @@
+"""CUDA path vs CPU oracle, element by element, through the C ABI.
+
+Plans, cu_seqlens, destinations and the inverse permutation must be
+bit-exact; the dispatch buffer and the prefetched slots are byte copies and
+must be bit-exact; GEMM and combine outputs must be within 1e-2 absolute +
+2e-2 relative of the oracle (bf16 values, fp32 accumulation); reduce_grad
+adds fp32 values in the oracle's order and must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import perfectly_balanced_token_gb300 as mx
+from oracle import layer as olayer
+from oracle import planner as oplanner
+from perfectly_balanced_token_gb300 import synthetic as syn
+from tests import gpu_harness as gh
+from tests.invariants import check_plan_arrays
+
+pytestmark = pytest.mark.gpu
+
+W = syn.Workload
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gh.ensure_library()
+
+
+# (workload, routing recipe) covering several GEMM column tiles (BN 64/128/256),
+# ragged row tails, tiles straddling ranks, K=1, R=1, E=R, inference overflow
+CASES = [
+    ("tiny", syn.TINY, lambda w: syn.routing_for(w)),
+    ("tiny-adversarial", syn.TINY, lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=2)),
+    ("r8e64-maxvio0", syn.SMALL, lambda w: syn.routing_for(w, 0.0)),
+    ("r8e64-maxvio1", syn.SMALL, lambda w: syn.routing_for(w, 1.0)),
+    ("r8e64-maxvio5", syn.SMALL, lambda w: syn.routing_for(w, 5.0)),
+    ("r1-single-rank", W("r1", R=1, E=4, B=4, K=2, S=37, H=64, Hp=64),
+     lambda w: syn.zipf_bias_routing(w.R, w.S, w.K, w.E, seed=4)),
+    ("r4-e4-k1-bn64", W("e=r", R=4, E=4, B=1, K=1, S=300, H=128, Hp=192),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=2.0, seed=5)),
+    ("r5-e20-ragged", W("ragged", R=5, E=20, B=4, K=3, S=171, H=192, Hp=320),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.3, seed=6)),
+    ("infer-b1-overflow", W("infer1", R=4, E=16, B=1, K=2, S=200, H=128, Hp=256, mode=1),
+     lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=4)),
+    ("infer-b0", W("infer0", R=4, E=16, B=0, K=2, S=96, H=64, Hp=128, mode=1),
+     lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=4)),
+    ("hot-rank-chain", W("chain", R=8, E=32, B=4, K=2, S=256, H=128, Hp=256),
+     lambda w: syn.Routing(((np.arange(w.R * w.S * w.K).reshape(w.R, w.S, w.K)) % 4).astype(np.int32),
+                           np.full((w.R, w.S, w.K), 0.5, np.float32))),
+]
+
+
+@pytest.mark.parametrize("name,w,mk", CASES, ids=[c[0] for c in CASES])
+def test_layer_parity(name, w, mk):
+    rt = mk(w)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt)
+    run.forward()
+
+    # plan: bit-exact, and Theorem 1 invariants on the GPU's own tables
+    tabs = run.ws.tables()
+    gh.compare_plan(tabs, fp, od)
+    check_plan_arrays(rt.idx, w.R, w.E, w.B, w.K, w.S, w.mode, T=tabs["T"],
+                      n_fills=int(tabs["counters"][0]), fills=tabs["fills"], keep=tabs["keep"],
+                      slot_expert=tabs["slot_expert"], n_recv=tabs["n_recv"], src=tabs["src"],
+                      cu_seqlens=tabs["cu_seqlens"], dst=tabs["dst"], inverse=tabs["inverse"],
+                      gidx=tabs["gidx"])
+
+    x_bits = gh.host_bits(run.x)
+    w_bits = gh.host_bits(run.w_home)
+    # dispatch: byte-exact copy of every token row to every destination
+    recv_want = olayer.permute(x_bits, fp["dst"], od)
+    assert np.array_equal(gh.host_bits(run.recv).reshape(w.N, w.H), recv_want)
+    # prefetch: occupied slots hold their expert's weights; empty slots untouched
+    if w.B:
+        ws = gh.host_bits(run.w_slot).reshape(w.R, w.B, w.H, w.Hp)
+        want = olayer.prefetch(w_bits, fp["plan"])
+        occ = fp["slot_expert"] >= 0
+        assert np.array_equal(ws[occ], want[occ])
+        assert np.all(ws[~occ] == 0x7F7F)
+    # GEMM: each copy's output row against the per-expert definition
+    per_e = olayer.expert_outputs(x_bits, w_bits, rt.idx, od)
+    y = gh.bf16_to_np(run.y).reshape(w.N, w.Hp)
+    dst = fp["dst"].reshape(-1)
+    for e, (cids, yb) in per_e.items():
+        if cids.size:
+            gh.assert_close(y[dst[cids]], gh.bits_to_np(yb), f"{name} Y expert {e}")
+    # combine: against the plan-free definition
+    out_want = olayer.combine_from_copies(per_e, rt.gates, od)
+    gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(out_want),
+                    f"{name} combine")
+    run.check_all_guards()
+
+
+@pytest.mark.parametrize("name,w,mk", CASES[:6], ids=[c[0] for c in CASES[:6]])
+def test_gemm_isolated_synthetic_rows(name, w, mk):
+    """GEMM on a synthetic receive buffer (not produced by dispatch)."""
+    rt = mk(w)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt)
+    run.plan()
+    recv = syn.normal_bf16((w.N, w.H), 1.0, 77).cuda()
+    mx.moonep_prefetch_weights(run.d, run.ws.buf, run.w_home, run.w_slot)
+    mx.moonep_grouped_gemm(run.d, run.ws.buf, recv.view(-1), run.w_home, run.w_slot, run.y)
+    want = olayer.grouped_gemm_rows(gh.host_bits(recv), fp["plan"], gh.host_bits(run.w_home))
+    gh.assert_close(gh.bf16_to_np(run.y).reshape(w.N, w.Hp), gh.bits_to_np(want), f"{name} gemm")
+
+
+@pytest.mark.parametrize("name,w,mk", CASES[:6], ids=[c[0] for c in CASES[:6]])
+def test_combine_isolated_synthetic_outputs(name, w, mk):
+    rt = mk(w)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt)
+    run.plan()
+    y = syn.normal_bf16((w.N, w.Hp), 1.0, 78).cuda()
+    mx.moonep_combine(run.d, run.ws.buf, y.view(-1), run.gates, run.out)
+    want = olayer.combine(gh.host_bits(y), fp["dst"], rt.gates, od)
+    gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(want),
+                    f"{name} combine")
+
+
+@pytest.mark.parametrize("name,w,mk", [c for c in CASES if c[1].B > 0],
+                         ids=[c[0] for c in CASES if c[1].B > 0])
+def test_reduce_grad_parity(name, w, mk):
+    rt = mk(w)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt)
+    run.plan()
+    hh = w.H * w.Hp
+    g_home = syn.normal_f32((w.E, w.H, w.Hp), 1.0, 90).cuda()
+    g_slot = syn.normal_f32((w.R, w.B, w.H, w.Hp), 1.0, 91).cuda()
+    occ = torch.from_numpy(fp["slot_expert"] >= 0).cuda()
+    g_slot[~occ] = 7.0  # sentinel: unoccupied slots must stay untouched
+    gh_host, gs_host = g_home.cpu().numpy().copy(), g_slot.cpu().numpy().copy()
+    mx.moonep_reduce_grad(run.d, run.ws.buf, g_home.view(-1), g_slot.view(-1))
+    olayer.reduce_grad(gh_host, gs_host, fp["plan"])
+    assert np.array_equal(g_home.cpu().numpy(), gh_host)
+    assert np.array_equal(g_slot.cpu().numpy(), gs_host)
+    assert bool((g_slot[occ] == 0).all()) and bool((g_slot[~occ] == 7.0).all())
+    assert hh > 0
+
+
+def test_determinism_two_runs():
+    w = syn.SMALL
+    rt = syn.routing_for(w, 5.0)
+    a, b = gh.Run(w, rt), gh.Run(w, rt)
+    a.forward()
+    b.forward()
+    assert torch.equal(a.ws.buf, b.ws.buf)
+    assert torch.equal(a.y, b.y) and torch.equal(a.out, b.out)
+
+
+def test_workspace_reuse_across_routings():
+    """A second plan in the same workspace fully replaces the first."""
+    w = syn.SMALL
+    r1, r2 = syn.routing_for(w, 5.0), syn.routing_for(w, 0.0)
+    run = gh.Run(w, r1)
+    run.plan()
+    run.idx.copy_(torch.from_numpy(r2.idx))
+    tabs = run.plan()
+    gh.compare_plan(tabs, oplanner.full_plan(r2.idx, gh.odims(w)), gh.odims(w))
+
+
+@pytest.mark.parametrize("bad", ["range", "duplicate"])
+def test_bad_routing_sets_status_and_writes_nothing(bad):
+    w = syn.TINY
+    f = syn.bad_routing_out_of_range if bad == "range" else syn.bad_routing_duplicate
+    rt = syn.Routing(f(w.R, w.S, w.K, w.E), np.full((w.R, w.S, w.K), 0.5, np.float32))
+    run = gh.Run(w, rt)
+    run.forward()  # every call after the plan sees the status and returns
+    st = mx.moonep_read_status(run.d, run.ws.buf)
+    assert st & mx._lib.ERR_ROUTING
+    for t in (run.recv, run.y, run.out):
+        assert bool((t.view(torch.int16) == 0x7F7F).all())
+    if w.B:
+        assert bool((run.w_slot.view(torch.int16) == 0x7F7F).all())
