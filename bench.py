@@ -1,0 +1,438 @@
+"""Benchmark of the MoonEP layer path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic routing:
+moonep_plan -> moonep_prefetch_weights -> moonep_dispatch -> moonep_grouped_gemm
+-> moonep_combine -> moonep_reduce_grad, all on one CUDA stream with every
+input already resident in HBM.  Timed steps rotate through the routing
+imbalance sweep maxvio in {0.2, 1, 10, 20} (the pages' benchmark setting,
+"Moonshot AI 开源 MoonEP", section 与 DeepEP v2 的基准测试), shape R=8 simulated
+ranks, E=384, B=48, K=8, S=8192, H=7168, H'=2048.
+
+Metric: routed token-copies per second, N = R*S*K copies per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the path has no data exchange on one GPU); rank 0 prints one
+JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed token-copies/sec (plan+permute+GEMM+combine) vs maxvio; % HBM & bf16 roofline"
+UNIT = "token-copies/s"
+SWEEP = (0.2, 1.0, 10.0, 20.0)
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (one all-reduce on a scalar); identity for one rank."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(w, maxvios):
+    return {"workload": f"{w.name}: R={w.R} E={w.E} B={w.B} K={w.K} S={w.S} H={w.H} H'={w.Hp}",
+            "R": w.R, "E": w.E, "B": w.B, "K": w.K, "S": w.S, "H": w.H, "Hp": w.Hp,
+            "mode": "training" if w.mode == 0 else "inference",
+            "maxvio_sweep": list(maxvios),
+            "step": "plan+prefetch+dispatch+grouped_gemm+combine+reduce_grad",
+            "l2": "256 MiB L2 flush write between timed steps; x, recv, W and grads exceed L2",
+            "parallelism": "replicas (R ranks simulated on each GPU)"}
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import perfectly_balanced_token_gb300 as mx
+    from perfectly_balanced_token_gb300 import synthetic as syn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mx.library()
+
+    w = syn.PAGES
+    sweep = tuple(args.maxvio) if args.maxvio else SWEEP
+    d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode)
+    N = w.N
+    st = torch.cuda.current_stream()
+
+    routings = [syn.routing_for(w, mv, seed=0) for mv in sweep]
+    measured_mv = [syn.input_skew(r.idx, w.E) for r in routings]
+    idx = [torch.from_numpy(r.idx).to(dev) for r in routings]
+    gates = [torch.from_numpy(r.gates).to(dev) for r in routings]
+    x = syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, dev)
+    w_home = syn.normal_bf16((w.E, w.H, w.Hp), 0.02, 2, dev)
+    w_slot = torch.zeros(w.R * w.B * w.H * w.Hp, dtype=torch.bfloat16, device=dev)
+    recv = torch.empty(N * w.H, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(N * w.Hp, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(w.R * w.S * w.Hp, dtype=torch.bfloat16, device=dev)
+    g_home = syn.normal_f32((w.E, w.H, w.Hp), 1.0, 3, dev)
+    g_slot = syn.normal_f32((w.R, w.B, w.H, w.Hp), 1.0, 4, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ws = mx.PlanWorkspace(d, device=dev)
+    names = ("plan", "prefetch", "dispatch", "gemm", "combine", "reduce_grad")
+
+    def step(i, ev=None):
+        j = i % len(sweep)
+        calls = (
+            lambda: mx.moonep_plan(d, idx[j], ws.buf, st),
+            lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot, st),
+            lambda: mx.moonep_dispatch(d, ws.buf, x, recv, st),
+            lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y, st),
+            lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out, st),
+            lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot, st),
+        )
+        for k, c in enumerate(calls):
+            if ev is not None:
+                ev[k].record(st)
+            c()
+        if ev is not None:
+            ev[len(calls)].record(st)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = mx.moonep_read_status(d, ws.buf)
+    if status:
+        raise RuntimeError(f"device status {status:#x}: {mx.status_string(status)}")
+
+    # per-maxvio plan counters (outside the timed region)
+    counters = []
+    for j in range(len(sweep)):
+        mx.moonep_plan(d, idx[j], ws.buf, st)
+        c = ws.view("counters", (8,)).cpu().tolist()
+        counters.append({"fills": c[0], "mtiles": c[1], "occupied_slots": c[2],
+                         "reduced_experts": c[3]})
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = mx.moonep_launch_count()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # evict L2 between steps (not inside a step's events)
+        step(i, evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = mx.moonep_launch_count() - launches0
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+
+    seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(6)]
+                    for i in range(args.steps)])  # ms
+    step_ms = seg.sum(axis=1)
+    total_ms = reduce_max(float(step_ms.sum()), world, dev)
+    headline_rows = [0, 2, 3, 4]
+    per_mv = []
+    for j, mv in enumerate(sweep):
+        rows = [i for i in range(args.steps) if i % len(sweep) == j]
+        if not rows:
+            continue
+        ms = float(step_ms[rows].mean())
+        hl = float(seg[rows][:, headline_rows].sum(axis=1).mean())
+        per_mv.append({"maxvio_target": mv, "maxvio": round(measured_mv[j], 4),
+                       "value": N / (ms / 1e3), "ms_per_step": ms,
+                       "value_plan_permute_gemm_combine": N / (hl / 1e3),
+                       "breakdown_ms": {n: float(seg[rows][:, k].mean()) for k, n in enumerate(names)},
+                       **counters[j]})
+
+    # e2e: host buffers through the same C ABI, copies inside the timed region
+    e2e = run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_slot, dev, st,
+                  world)
+
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gemm_ms = float(seg[:, 3].mean())
+    flops = 2.0 * N * w.H * w.Hp
+    achieved_tf = flops / (gemm_ms / 1e3) / 1e12
+    roofline = {"kernel": "k_ggemm (moonep_grouped_gemm)", "bound": "tensor",
+                "achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved_tf / bf16_peak, "peak_source": f"bf16_tflops ({peak_src}, burst)",
+                "traffic": None, "algorithmic_flops_per_launch": flops,
+                "ms_per_launch": gemm_ms}
+    occ = np.mean([c["occupied_slots"] for c in counters])
+    red = np.mean([c["reduced_experts"] for c in counters])
+    hh = w.H * w.Hp
+    algo_bytes = {
+        "dispatch": w.R * w.S * w.H * 2 + N * w.H * 2 + N * 4,
+        "combine": N * w.Hp * 2 + N * 8 + w.R * w.S * w.Hp * 2,
+        "prefetch": occ * hh * 2 * 2,
+        "reduce_grad": (occ + red) * hh * 4 * 2,
+    }
+    col = {"dispatch": 2, "combine": 4, "prefetch": 1, "reduce_grad": 5}
+    rooflines = {}
+    for k, b in algo_bytes.items():
+        ms = float(seg[:, col[k]].mean())
+        gbs = b / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+        rooflines[k] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": gbs / hbm_peak, "bytes_per_launch": b, "ms_per_launch": ms}
+    rooflines["plan"] = {"bound": "latency", "us_per_launch": float(seg[:, 0].mean()) * 1e3}
+
+    result = {
+        "metric": METRIC, "value": N * args.steps * world / (total_ms / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, sweep),
+        "value_plan_permute_gemm_combine": N * args.steps * world /
+        (reduce_max(float(seg[:, headline_rows].sum()), world, dev) / 1e3),
+        "sweep": per_mv, "e2e": e2e, "gpu_launches": launches,
+        "roofline": roofline, "rooflines": rooflines, "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_slot, dev, st,
+            world):
+    """Same step, but x / routing / gates start in pinned host memory and the
+    combined output is read back to pinned host memory every step."""
+    N = w.N
+    x_h = syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, "cpu").pin_memory()
+    idx_h = [torch.from_numpy(r.idx).pin_memory() for r in routings]
+    g_h = [torch.from_numpy(r.gates).pin_memory() for r in routings]
+    out_h = torch.empty(w.R * w.S * w.Hp, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x_h, device=dev)
+    idx_d = torch.empty_like(idx_h[0], device=dev)
+    g_d = torch.empty_like(g_h[0], device=dev)
+    recv = torch.empty(N * w.H, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(N * w.Hp, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(w.R * w.S * w.Hp, dtype=torch.bfloat16, device=dev)
+    steps = max(2, min(args.steps, 8))
+
+    def one(i):
+        j = i % len(routings)
+        x_d.copy_(x_h, non_blocking=True)
+        idx_d.copy_(idx_h[j], non_blocking=True)
+        g_d.copy_(g_h[j], non_blocking=True)
+        mx.moonep_plan(d, idx_d, ws.buf, st)
+        mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot, st)
+        mx.moonep_dispatch(d, ws.buf, x_d, recv, st)
+        mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y, st)
+        mx.moonep_combine(d, ws.buf, y, g_d, out, st)
+        mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot, st)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        one(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world, dev)
+    h2d = x_h.numel() * 2 + idx_h[0].numel() * 4 + g_h[0].numel() * 4
+    return {"value": N * steps * world / (ms / 1e3), "unit": UNIT, "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel() * 2)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(budget_s: float, seed: int = 0):
+    """Time the oracle (as it stands) on a bounded sample of the workload.
+
+    Sample: the full plan (histogram, constructive plan, every destination)
+    over all N copies of one maxvio=1 routing, then permute + expert GEMM +
+    combine for the copies of a few experts, scaled to all N copies by copy
+    count.  Returns (copies_per_s, description, seconds spent)."""
+    import torch
+
+    from oracle import layer as olayer
+    from oracle import planner as oplanner
+    from perfectly_balanced_token_gb300 import synthetic as syn
+
+    w = syn.PAGES
+    od = oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp)
+    rt = syn.routing_for(w, 1.0, seed=seed)
+    t0 = time.perf_counter()
+    fp = oplanner.full_plan(rt.idx, od)
+    t_plan = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    flat = rt.idx.reshape(-1)
+    copies, t_rest, experts = 0, 0.0, []
+    x_all = None
+    while t_plan + t_rest < budget_s and len(experts) < w.E:
+        e = int(rng.integers(0, w.E))
+        if e in experts:
+            continue
+        experts.append(e)
+        if x_all is None:
+            x_all = syn.bf16_bits(syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, "cpu"))
+        wb = syn.bf16_bits(syn.normal_bf16((w.H, w.Hp), 0.02, 100 + e, "cpu"))
+        cids = np.nonzero(flat == e)[0]
+        t1 = time.perf_counter()
+        rows = olayer.bf16_to_f64(x_all.reshape(-1, w.H)[cids // w.K])   # permute (gather)
+        yb = olayer.to_bf16(rows @ olayer.bf16_to_f64(wb))              # expert GEMM
+        g = rt.gates.reshape(-1)[cids].astype(np.float64)[:, None]      # combine share
+        _ = olayer.to_bf16(g * olayer.bf16_to_f64(yb))
+        t_rest += time.perf_counter() - t1
+        copies += cids.size
+    per_copy = t_plan / w.N + t_rest / max(copies, 1)
+    desc = (f"oracle full plan over all {w.N} copies (maxvio 1) in {t_plan:.2f} s; permute+GEMM+"
+            f"combine for {copies} copies of {len(experts)} experts in {t_rest:.2f} s; "
+            f"scaled per copy")
+    del torch
+    return 1.0 / per_copy, desc, t_plan + t_rest
+
+
+def cpu_baseline(budget_s: float):
+    v, desc, _ = oracle_sample(budget_s)
+    return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": desc, "threads_note": "NumPy BLAS with its default thread count"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import perfectly_balanced_token_gb300.synthetic as syn
+    w = syn.PAGES
+    budget = max(2.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(budget, seed=0)
+    vals, spent = [], 0.0
+    for i in range(args.steps):
+        v, desc, s = oracle_sample(budget, seed=0)
+        vals.append(v)
+        spent += s
+    v = float(np.mean(vals))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.N / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, (1.0,)),
+        "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "sample": desc, "value": v},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--maxvio", type=float, nargs="*", default=None)
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
