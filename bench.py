@@ -337,55 +337,60 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
 # ----------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample(budget_s: float, seed: int = 0):
+class OracleSample:
     """Time the oracle (as it stands) on a bounded sample of the workload.
 
     Sample: the full plan (histogram, constructive plan, every destination)
     over all N copies of one maxvio=1 routing, then permute + expert GEMM +
     combine for the copies of a few experts, scaled to all N copies by copy
-    count.  Returns (copies_per_s, description, seconds spent)."""
-    import torch
+    count.  Inputs are drawn once; run() returns (copies_per_s, description,
+    seconds spent)."""
 
-    from oracle import layer as olayer
-    from oracle import planner as oplanner
-    from perfectly_balanced_token_gb300 import synthetic as syn
+    def __init__(self, seed: int = 0):
+        from oracle import planner as oplanner
+        from perfectly_balanced_token_gb300 import synthetic as syn
 
-    w = syn.PAGES
-    od = oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp)
-    rt = syn.routing_for(w, 1.0, seed=seed)
-    t0 = time.perf_counter()
-    fp = oplanner.full_plan(rt.idx, od)
-    t_plan = time.perf_counter() - t0
-    rng = np.random.default_rng(seed)
-    flat = rt.idx.reshape(-1)
-    copies, t_rest, experts = 0, 0.0, []
-    x_all = None
-    while t_plan + t_rest < budget_s and len(experts) < w.E:
-        e = int(rng.integers(0, w.E))
-        if e in experts:
-            continue
-        experts.append(e)
-        if x_all is None:
-            x_all = syn.bf16_bits(syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, "cpu"))
-        wb = syn.bf16_bits(syn.normal_bf16((w.H, w.Hp), 0.02, 100 + e, "cpu"))
-        cids = np.nonzero(flat == e)[0]
-        t1 = time.perf_counter()
-        rows = olayer.bf16_to_f64(x_all.reshape(-1, w.H)[cids // w.K])   # permute (gather)
-        yb = olayer.to_bf16(rows @ olayer.bf16_to_f64(wb))              # expert GEMM
-        g = rt.gates.reshape(-1)[cids].astype(np.float64)[:, None]      # combine share
-        _ = olayer.to_bf16(g * olayer.bf16_to_f64(yb))
-        t_rest += time.perf_counter() - t1
-        copies += cids.size
-    per_copy = t_plan / w.N + t_rest / max(copies, 1)
-    desc = (f"oracle full plan over all {w.N} copies (maxvio 1) in {t_plan:.2f} s; permute+GEMM+"
-            f"combine for {copies} copies of {len(experts)} experts in {t_rest:.2f} s; "
-            f"scaled per copy")
-    del torch
-    return 1.0 / per_copy, desc, t_plan + t_rest
+        self.w = w = syn.PAGES
+        self.od = oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp)
+        self.rt = syn.routing_for(w, 1.0, seed=seed)
+        self.x = syn.bf16_bits(syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, "cpu")).reshape(-1, w.H)
+        self.seed = seed
+
+    def run(self, budget_s: float):
+        from oracle import layer as olayer
+        from oracle import planner as oplanner
+        from perfectly_balanced_token_gb300 import synthetic as syn
+
+        w = self.w
+        t0 = time.perf_counter()
+        oplanner.full_plan(self.rt.idx, self.od)
+        t_plan = time.perf_counter() - t0
+        rng = np.random.default_rng(self.seed)
+        flat = self.rt.idx.reshape(-1)
+        copies, t_rest, experts = 0, 0.0, []
+        while t_plan + t_rest < budget_s and len(experts) < w.E:
+            e = int(rng.integers(0, w.E))
+            if e in experts:
+                continue
+            experts.append(e)
+            wb = syn.bf16_bits(syn.normal_bf16((w.H, w.Hp), 0.02, 100 + e, "cpu"))
+            cids = np.nonzero(flat == e)[0]
+            t1 = time.perf_counter()
+            rows = olayer.bf16_to_f64(self.x[cids // w.K])                  # permute (gather)
+            yb = olayer.to_bf16(rows @ olayer.bf16_to_f64(wb))              # expert GEMM
+            g = self.rt.gates.reshape(-1)[cids].astype(np.float64)[:, None]  # combine share
+            olayer.to_bf16(g * olayer.bf16_to_f64(yb))
+            t_rest += time.perf_counter() - t1
+            copies += cids.size
+        per_copy = t_plan / w.N + t_rest / max(copies, 1)
+        desc = (f"oracle full plan over all {w.N} copies (maxvio 1) in {t_plan:.2f} s; "
+                f"permute+GEMM+combine for {copies} copies of {len(experts)} experts in "
+                f"{t_rest:.2f} s; scaled per copy")
+        return 1.0 / per_copy, desc, t_plan + t_rest
 
 
 def cpu_baseline(budget_s: float):
-    v, desc, _ = oracle_sample(budget_s)
+    v, desc, _ = OracleSample().run(budget_s)
     return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": desc, "threads_note": "NumPy BLAS with its default thread count"}
 
@@ -397,11 +402,12 @@ def run_reference(args):
     import perfectly_balanced_token_gb300.synthetic as syn
     w = syn.PAGES
     budget = max(2.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
+    sample = OracleSample()
     for _ in range(args.warmup):
-        oracle_sample(budget, seed=0)
+        sample.run(budget)
     vals, spent = [], 0.0
     for i in range(args.steps):
-        v, desc, s = oracle_sample(budget, seed=0)
+        v, desc, s = sample.run(budget)
         vals.append(v)
         spent += s
     v = float(np.mean(vals))

@@ -1,0 +1,56 @@
+"""Host logic of bench.py without a GPU: the N>1 replica path's max-over-ranks
+timing (world size 2 over gloo), argument handling and peak lookup."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
+    w, r, loc = bench.dist_env()
+    got = bench.reduce_max(10.0 * (rank + 1), w, "cpu")
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((r, w, loc, got))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2, 0, 20.0), (1, 2, 1, 20.0)]
+
+
+def test_single_rank_is_identity():
+    assert bench.reduce_max(3.5, 1, "cpu") == 3.5
+
+
+def test_warmup_must_be_at_least_three():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
+
+
+def test_peaks_lookup_has_the_denominators():
+    peaks, src = bench.load_peaks()
+    assert src in ("measured", "fallback")
+    assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 500
