@@ -39,6 +39,26 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def _profile_workload():
+    from perfectly_balanced_token_gb300 import synthetic as syn
+    # the pages shape's H, H', K with fewer experts and tokens: a few GB on the device
+    return syn.Workload("profile-sized", R=8, E=32, B=4, K=8, S=1024, H=7168, Hp=2048)
+
+
+def _pages():
+    from perfectly_balanced_token_gb300 import synthetic as syn
+    return syn.PAGES
+
+
+def _k3():
+    from perfectly_balanced_token_gb300 import synthetic as syn
+    return syn.K3
+
+
+WORKLOADS = {"pages": _pages, "k3": _k3, "profile": _profile_workload}
+DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,)}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -144,8 +164,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     mx.library()
 
-    w = syn.PAGES
-    sweep = tuple(args.maxvio) if args.maxvio else SWEEP
+    w = WORKLOADS[args.workload]()
+    sweep = tuple(args.maxvio) if args.maxvio else DEFAULT_SWEEP.get(args.workload, SWEEP)
     d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode)
     N = w.N
     st = torch.cuda.current_stream()
@@ -236,8 +256,8 @@ def run_ours(args):
                        **counters[j]})
 
     # e2e: host buffers through the same C ABI, copies inside the timed region
-    e2e = run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_slot, dev, st,
-                  world)
+    e2e = None if args.no_e2e else run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot,
+                                            g_home, g_slot, dev, st, world)
 
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -280,7 +300,7 @@ def run_ours(args):
         "roofline": roofline, "rooflines": rooflines, "clocks": clk,
         "wall_s_timed_region": t_wall,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "pages":
         result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if world > 1:
         import torch.distributed as dist
@@ -431,6 +451,10 @@ def main(argv=None):
     ap.add_argument("--maxvio", type=float, nargs="*", default=None)
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pages",
+                    help="pages = the headline configuration; the others are smaller cases "
+                         "of the same kernels for profiling")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

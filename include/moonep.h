@@ -56,6 +56,8 @@ enum moonep_status {
   MOONEP_ERR_SHAPE = 4,    /* E % R != 0, K > E, E > 4096, H or Hp not a multiple
                               of 64, or N, R*B*H or E*H reaches 2^31            */
   MOONEP_ERR_CUDA = 5,     /* a CUDA runtime call or launch failed             */
+  MOONEP_ERR_SCRATCH = 6,  /* moonep_plan_noalloc: the dims need more planner
+                              scratch than its fixed static capacity            */
   /* device-detected bits, OR-ed into the workspace status word */
   MOONEP_ERR_ROUTING = 0x100,  /* an expert id outside [0,E) or repeated within a token */
   MOONEP_ERR_INTERNAL = 0x200, /* a planner invariant failed (cannot happen for valid routing) */
@@ -186,6 +188,37 @@ const char* moonep_status_string(int status);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t moonep_launch_count(void);
+
+/* moonep_plan for callers that cannot allocate device memory.
+ *
+ * There is no counterpart on the pages: this is an operational variant.  Some
+ * callers cannot call cudaMalloc at planning time -- for example code running
+ * inside a pre-sized memory pool or arena that must not grow, a caching
+ * allocator that forbids new allocations after warm-up, or a runtime that
+ * plans between captured graph segments.  This entry point computes exactly
+ * what moonep_plan computes (same workspace layout, same output tables, bit
+ * for bit) but keeps the planner's internal scratch -- the per-chunk expert
+ * counts, the per-expert migrated ranges and their row bases, and the per-rank
+ * tile offsets -- in one file-scope static device array of 4 MiB
+ * (MOONEP_NOALLOC_SCRATCH_BYTES) instead of in plan_ws.  The array is part of
+ * the library's device image: every GPU that loads the library holds it until
+ * the process exits, and nothing is ever allocated or freed by this call (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *
+ * Arguments are those of moonep_plan; plan_ws still receives every output
+ * table (its internal scratch regions are left untouched).  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the one array, which keeps the last call's contents:
+ * calls whose kernels overlap on the GPU (two streams, or two host threads)
+ * race on it and must be serialised by the caller.  Every scratch entry a
+ * call reads is written earlier in the same call, so no clearing is needed.
+ * Returns MOONEP_ERR_SCRATCH, before anything is enqueued, when the dims need
+ * more than the capacity (roughly 4*(R*ceil(S/ceil(4096/K))*E + 5*E*R + E)
+ * bytes plus alignment). */
+#define MOONEP_NOALLOC_SCRATCH_BYTES (4u << 20)
+int moonep_plan_noalloc(const moonep_dims* dims, const int32_t* topk_idx, void* plan_ws,
+                        void* stream);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmoonep.so")
 
 OK = 0
-ERR_ARG, ERR_ALIGN, ERR_SLOTS, ERR_SHAPE, ERR_CUDA = 1, 2, 3, 4, 5
+ERR_ARG, ERR_ALIGN, ERR_SLOTS, ERR_SHAPE, ERR_CUDA, ERR_SCRATCH = 1, 2, 3, 4, 5, 6
 ERR_ROUTING, ERR_INTERNAL, ERR_TIMEOUT = 0x100, 0x200, 0x400
 CNT_FILLS, CNT_MTILES, CNT_OCCUPIED, CNT_REDUCE = 0, 1, 2, 3
 
@@ -78,6 +78,7 @@ def library() -> ctypes.CDLL:
         "moonep_reduce_grad": [D, P, P, P, P],
         "moonep_read_status": [D, P, ctypes.POINTER(ctypes.c_int32), P],
         "moonep_plan_export": [D, P, P, P],
+        "moonep_plan_noalloc": [D, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -152,6 +153,14 @@ def _ws(d, ws):
 def moonep_plan(d, topk_idx, plan_ws, stream=None):
     _check(library().moonep_plan(ctypes.byref(d), _ptr(topk_idx, torch.int32, d.N, "topk_idx"),
                                  _ws(d, plan_ws), _stream(stream)), "moonep_plan")
+
+
+def moonep_plan_noalloc(d, topk_idx, plan_ws, stream=None):
+    """moonep_plan with the planner's scratch in the library's static device
+    array (nothing allocated); same outputs in plan_ws."""
+    _check(library().moonep_plan_noalloc(ctypes.byref(d),
+                                         _ptr(topk_idx, torch.int32, d.N, "topk_idx"),
+                                         _ws(d, plan_ws), _stream(stream)), "moonep_plan_noalloc")
 
 
 def moonep_prefetch_weights(d, plan_ws, w_home, w_slot, stream=None):

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -260,6 +261,7 @@ const char* moonep_status_string(int s) {
     case MOONEP_ERR_SLOTS: return "training mode needs B >= E/R prefetch slots";
     case MOONEP_ERR_SHAPE: return "unsupported shape (E%R, K>E, E>4096, B>E, H or Hp not a multiple of 64, or a size >= 2^31)";
     case MOONEP_ERR_CUDA: return "CUDA runtime error or launch failure";
+    case MOONEP_ERR_SCRATCH: return "dims need more planner scratch than the fixed no-allocation capacity (4 MiB)";
     default: break;
   }
   if (s & MOONEP_ERR_ROUTING) return "device: expert id out of range or repeated within a token";
@@ -271,3 +273,84 @@ const char* moonep_status_string(int s) {
 uint64_t moonep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moonep_plan_noalloc: the planner with its internal scratch in a static
+// device array, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace moonep {
+
+constexpr size_t kNoAllocBytes = MOONEP_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+// Lives in the library's device image on every GPU that loads it; host code
+// must not use this name as an address (it is a host-side stand-in).
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocBytes / sizeof(int32_t)];
+
+static std::mutex g_noalloc_mutex;
+static void* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+static int noalloc_base(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return MOONEP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_base[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOONEP_ERR_CUDA;
+    g_noalloc_base[dev] = p;
+  }
+  *out = g_noalloc_base[dev];
+  return MOONEP_OK;
+}
+
+// Offsets of the planner's internal tables inside the static array.
+struct NoAllocLayout {
+  size_t counts, pieces, piece_n, piece_base, home_base, rank_tiles, total;
+};
+
+static NoAllocLayout noalloc_layout(const Dims& d) {
+  NoAllocLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + std::max<size_t>(bytes, 4));
+    return at;
+  };
+  const size_t R = d.R, E = d.E;
+  L.counts = take(4 * R * d.nchunk * E);
+  L.pieces = take(sizeof(Piece) * E * R);
+  L.piece_n = take(4 * E);
+  L.piece_base = take(4 * E * R);
+  L.home_base = take(4 * E);
+  L.rank_tiles = take(4 * (R + 1));
+  L.total = off;
+  return L;
+}
+
+}  // namespace moonep
+
+extern "C" int moonep_plan_noalloc(const moonep_dims* dims, const int32_t* topk_idx,
+                                   void* plan_ws, void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(topk_idx);
+  const NoAllocLayout S = noalloc_layout(d);
+  if (S.total > kNoAllocBytes) return MOONEP_ERR_SCRATCH;
+  void* base = nullptr;
+  const int rc = noalloc_base(&base);
+  if (rc != MOONEP_OK) return rc;
+  char* b = static_cast<char*>(base);
+  PlanPtrs Q = P;
+  Q.counts = (int32_t*)(b + S.counts);
+  Q.pieces = (Piece*)(b + S.pieces);
+  Q.piece_n = (int32_t*)(b + S.piece_n);
+  Q.piece_base = (int32_t*)(b + S.piece_base);
+  Q.home_base = (int32_t*)(b + S.home_base);
+  Q.rank_tiles = (int32_t*)(b + S.rank_tiles);
+  int n = 0;
+  const cudaError_t e = launch_plan(d, topk_idx, Q, (cudaStream_t)stream, &n);
+  return finish(e, n);
+}

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -101,8 +101,19 @@ def test_bad_pointers_rejected_before_launch(lib):
     assert mx.moonep_launch_count() == n0
 
 
+def test_noalloc_planner_rejects_dims_beyond_its_scratch(lib):
+    # R*nchunk*E = 64*10*4096 chunk counters alone exceed the 4 MiB array
+    n0 = mx.moonep_launch_count()
+    big = mx.dims(64, 4096, 64, 1, 40960, 64, 64)
+    rc = lib.moonep_plan_noalloc(ctypes.byref(big), ctypes.c_void_p(0x20000),
+                                 ctypes.c_void_p(0x10000), None)
+    assert rc == _lib.ERR_SCRATCH
+    assert "scratch" in mx.status_string(rc)
+    assert mx.moonep_launch_count() == n0
+
+
 def test_status_strings():
-    for code in (0, 1, 2, 3, 4, 5, 0x100, 0x200, 0x400, 0x300):
+    for code in (0, 1, 2, 3, 4, 5, 6, 0x100, 0x200, 0x400, 0x300):
         s = mx.status_string(code)
         assert s and s != "unknown status"
 
