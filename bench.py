@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def _profile_workload():
     from perfectly_balanced_token_gb300 import synthetic as syn
     # the pages shape's H, H', K with fewer experts and tokens: a few GB on the device
-    return syn.Workload("profile-sized", R=8, E=32, B=4, K=8, S=1024, H=7168, Hp=2048)
+    return syn.Workload("profile-sized", R=8, E=16, B=2, K=8, S=1024, H=7168, Hp=2048)
 
 
 def _pages():
@@ -100,13 +100,18 @@ def workload_config(w, maxvios):
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampled every 200 ms.  Started before the warm-up (its own
+    start-up must not overlap the timed region); summary() keeps only the
+    samples taken inside the timed window."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
+        self.lines = []
 
     def start(self):
         try:
@@ -119,26 +124,34 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return None
-        time.sleep(0.25)
+            return
+        time.sleep(0.3)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        self.lines = out.strip().splitlines()
+        self.proc = None
+
+    def summary(self, t0: float, t1: float):
+        import datetime
         sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+        for line in self.lines:
+            parts = [q.strip() for q in line.split(",")]
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            if not (t0 - 0.25 <= ts <= t1 + 0.25):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(self.REASONS, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
@@ -186,25 +199,22 @@ def run_ours(args):
     ws = mx.PlanWorkspace(d, device=dev)
     names = ("plan", "prefetch", "dispatch", "gemm", "combine", "reduce_grad")
 
-    def step(i, ev=None):
-        j = i % len(sweep)
-        calls = (
-            lambda: mx.moonep_plan(d, idx[j], ws.buf, st),
-            lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot, st),
-            lambda: mx.moonep_dispatch(d, ws.buf, x, recv, st),
-            lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y, st),
-            lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out, st),
-            lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot, st),
+    def calls(j):
+        # stream=None: the current stream (the capture stream while capturing)
+        return (
+            lambda: mx.moonep_plan(d, idx[j], ws.buf),
+            lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot),
+            lambda: mx.moonep_dispatch(d, ws.buf, x, recv),
+            lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y),
+            lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out),
+            lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot),
         )
-        for k, c in enumerate(calls):
-            if ev is not None:
-                ev[k].record(st)
-            c()
-        if ev is not None:
-            ev[len(calls)].record(st)
 
+    clocks = ClockSampler(local)
+    clocks.start()  # before the warm-up, so nvidia-smi's start-up is over by the timed region
     for i in range(args.warmup):
-        step(i)
+        for c in calls(i % len(sweep)):
+            c()
     torch.cuda.synchronize()
     status = mx.moonep_read_status(d, ws.buf)
     if status:
@@ -218,24 +228,50 @@ def run_ours(args):
         counters.append({"fills": c[0], "mtiles": c[1], "occupied_slots": c[2],
                          "reduced_experts": c[3]})
 
+    # one CUDA graph per (routing, segment): the timed loop only replays graphs, so
+    # host-side enqueue cost never shows up between the per-segment events
+    graphs, graph_launches = [], []
+    for j in range(len(sweep)):
+        gj, lj = [], []
+        for c in calls(j):
+            g = torch.cuda.CUDAGraph()
+            n0 = mx.moonep_launch_count()
+            with torch.cuda.graph(g):
+                c()
+            lj.append(mx.moonep_launch_count() - n0)
+            gj.append(g)
+        graphs.append(gj)
+        graph_launches.append(lj)
+    for j in range(len(sweep)):  # first replay uploads each graph
+        for g in graphs[j]:
+            g.replay()
+    torch.cuda.synchronize()
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    launches0 = mx.moonep_launch_count()
+    launches = 0
     t_wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     for i in range(args.steps):
+        j = i % len(sweep)
         flush.fill_(float(i))  # evict L2 between steps (not inside a step's events)
-        step(i, evs[i])
+        for k in range(6):
+            evs[i][k].record()
+            graphs[j][k].replay()
+        evs[i][6].record()
+        launches += sum(graph_launches[j])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    launches = mx.moonep_launch_count() - launches0
-    clk = clocks.stop()
+    t_epoch1 = time.time()
     if world > 1:
         dist.barrier()
+    status = mx.moonep_read_status(d, ws.buf)
+    if status:
+        raise RuntimeError(f"device status after the timed steps {status:#x}: "
+                           f"{mx.status_string(status)}")
 
     seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(6)]
                     for i in range(args.steps)])  # ms
@@ -258,6 +294,8 @@ def run_ours(args):
     # e2e: host buffers through the same C ABI, copies inside the timed region
     e2e = None if args.no_e2e else run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot,
                                             g_home, g_slot, dev, st, world)
+    clocks.stop()
+    clk = clocks.summary(t_epoch0, t_epoch1)
 
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -298,7 +336,9 @@ def run_ours(args):
         (reduce_max(float(seg[:, headline_rows].sum()), world, dev) / 1e3),
         "sweep": per_mv, "e2e": e2e, "gpu_launches": launches,
         "roofline": roofline, "rooflines": rooflines, "clocks": clk,
-        "wall_s_timed_region": t_wall,
+        "wall_s_timed_region": t_wall, "timing": "CUDA events between CUDA-graph replays of each "
+        "segment on the launching stream; gpu_launches counted from the captured graphs",
+        "step_ms": [float(v) for v in step_ms],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "pages":
         result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)

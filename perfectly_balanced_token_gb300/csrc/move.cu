@@ -135,52 +135,69 @@ k_combine(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restri
 // ---------------------------------------------------------------------------
 // reduce_grad: g_home[e] += g_slot[s] for the slots s holding e (ascending),
 // then g_slot[s] = 0 ("Moonshot AI 开源 MoonEP", contract paragraph)
+//
+// A work item is a 256 KiB span of one expert's rows; its slot list is read
+// once into shared memory, then the span is walked in 32 KiB sub-chunks with
+// 8 float4 of the home row and 8 of a slot in flight per thread.
 // ---------------------------------------------------------------------------
-constexpr int kRedVec = 4;                                 // float4 per thread per item
-constexpr int kRedChunk = kCopyThreads * kRedVec;          // float4 per work item
+constexpr int kRedVec = 8;                                 // float4 per thread per sub-chunk
+constexpr int kRedSub = kCopyThreads * kRedVec;            // float4 per sub-chunk
+constexpr int kRedSpan = 8;                                // sub-chunks per work item
 
 __global__ void __launch_bounds__(kCopyThreads)
 k_reduce(Dims d, PlanPtrs p, float4* __restrict__ g_home, float4* __restrict__ g_slot) {
+  extern __shared__ int32_t s_slots[];  // [R]: slots of the current expert
   if (plan_failed(p.status)) return;
   const size_t v_per = (size_t)d.H * d.Hp / 4;
-  const int nch = (int)((v_per + kRedChunk - 1) / kRedChunk);
-  const int items = p.counters[MOONEP_CNT_REDUCE] * nch;
+  const size_t span = (size_t)kRedSub * kRedSpan;
+  const int nsp = (int)((v_per + span - 1) / span);
+  const int items = p.counters[MOONEP_CNT_REDUCE] * nsp;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int e = p.red_list[it / nch];
+    const int e = p.red_list[it / nsp];
     const int n = p.red_n[e];
-    const int32_t* slots = p.red_slots + (size_t)e * d.R;
-    const size_t v0 = (size_t)(it % nch) * kRedChunk;
+    __syncthreads();  // the previous item is done with s_slots
+    for (int j = threadIdx.x; j < n; j += kCopyThreads) s_slots[j] = p.red_slots[(size_t)e * d.R + j];
+    __syncthreads();
     float4* home = g_home + (size_t)e * v_per;
-    float4 acc[kRedVec];
-#pragma unroll
-    for (int i = 0; i < kRedVec; ++i) {
-      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
-      if (a < v_per) acc[i] = __ldcs(home + a);
-    }
-    for (int j = 0; j < n; ++j) {
-      float4* sl = g_slot + (size_t)slots[j] * v_per;
-      float4 v[kRedVec];
+    const size_t s0 = (size_t)(it % nsp) * span;
+    const size_t s1 = s0 + span < v_per ? s0 + span : v_per;
+    for (size_t v0 = s0; v0 < s1; v0 += kRedSub) {
+      float4 acc[kRedVec], v[kRedVec];
+      float4* sl = g_slot + (size_t)s_slots[0] * v_per;
 #pragma unroll
       for (int i = 0; i < kRedVec; ++i) {
         const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
-        if (a < v_per) v[i] = __ldcs(sl + a);
-      }
-#pragma unroll
-      for (int i = 0; i < kRedVec; ++i) {
-        const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
-        if (a < v_per) {
-          acc[i].x = acc[i].x + v[i].x;
-          acc[i].y = acc[i].y + v[i].y;
-          acc[i].z = acc[i].z + v[i].z;
-          acc[i].w = acc[i].w + v[i].w;
-          __stcs(sl + a, make_float4(0.f, 0.f, 0.f, 0.f));
+        if (a < s1) {
+          acc[i] = __ldcs(home + a);
+          v[i] = __ldcs(sl + a);
         }
       }
-    }
+      for (int j = 0; j < n; ++j) {
+        if (j > 0) {
+          sl = g_slot + (size_t)s_slots[j] * v_per;
 #pragma unroll
-    for (int i = 0; i < kRedVec; ++i) {
-      const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
-      if (a < v_per) __stcs(home + a, acc[i]);
+          for (int i = 0; i < kRedVec; ++i) {
+            const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+            if (a < s1) v[i] = __ldcs(sl + a);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kRedVec; ++i) {
+          const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+          if (a < s1) {
+            acc[i].x = acc[i].x + v[i].x;
+            acc[i].y = acc[i].y + v[i].y;
+            acc[i].z = acc[i].z + v[i].z;
+            acc[i].w = acc[i].w + v[i].w;
+            __stcs(sl + a, make_float4(0.f, 0.f, 0.f, 0.f));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRedVec; ++i) {
+        const size_t a = v0 + threadIdx.x + (size_t)i * kCopyThreads;
+        if (a < s1) __stcs(home + a, acc[i]);
+      }
     }
   }
 }
@@ -242,7 +259,7 @@ cudaError_t launch_reduce(const Dims& d, const PlanPtrs& p, float* g_home, float
                           cudaStream_t st, int* launches) {
   if (d.B == 0) return cudaSuccess;
   const int grid = sm_count() * 8;
-  k_reduce<<<grid, kCopyThreads, 0, st>>>(d, p, (float4*)g_home, (float4*)g_slot);
+  k_reduce<<<grid, kCopyThreads, sizeof(int32_t) * d.R, st>>>(d, p, (float4*)g_home, (float4*)g_slot);
   *launches += 1;
   return cudaGetLastError();
 }
