@@ -85,17 +85,22 @@ typedef struct moonep_plan_layout {
   size_t pieces;       /* internal: per-expert ranges of ordinals and their rows */
   size_t occupied;     /* int32[R*B] occupied slot ids u*B+j, ascending          */
   size_t reduce;       /* internal: per-expert slot lists for reduce_grad        */
-  size_t mtiles;       /* internal: 128-row GEMM tiles (int32[4] each)           */
+  size_t mtiles;       /* internal: 256-row GEMM work tiles (int32[4] each)      */
   int32_t nchunk;      /* token chunks per rank used by the histogram            */
   int32_t max_mtiles;
+  size_t route;        /* int32[R][S][K] send-once route entries: the copy's row
+                          offset on its destination rank, or -offset-1 when an
+                          earlier entry of the same token already goes there  */
 } moonep_plan_layout;
 
 /* Index of each counter in the `counters` table. */
 enum moonep_counter {
   MOONEP_CNT_FILLS = 0,    /* fills performed (<= R-1)                     */
-  MOONEP_CNT_MTILES = 1,   /* 128-row GEMM tiles over all ranks and groups */
+  MOONEP_CNT_MTILES = 1,   /* 256-row GEMM work tiles over all ranks and groups */
   MOONEP_CNT_OCCUPIED = 2, /* occupied prefetch slots                      */
-  MOONEP_CNT_REDUCE = 3    /* home experts with at least one slot copy     */
+  MOONEP_CNT_REDUCE = 3,   /* home experts with at least one slot copy     */
+  MOONEP_CNT_REMOTE_ENTRIES = 4, /* route entries whose destination is not the token's own rank */
+  MOONEP_CNT_REMOTE_PAIRS = 5    /* distinct (token, destination rank) pairs among those       */
 };
 
 /* Size in bytes of the plan workspace for `dims` (host only, no CUDA call).
@@ -143,6 +148,24 @@ int moonep_prefetch_weights(const moonep_dims* dims, void* plan_ws,
 int moonep_dispatch(const moonep_dims* dims, void* plan_ws, const uint16_t* x,
                     uint16_t* recv, void* stream);
 
+/* Send-once dispatch ("Kimi K3 模型结构（8）", section 在线规划、零拷贝、静态 shape:
+ * several of a token's K routes often land on the same rank, which needs the
+ * token vector only once; a route entry holds its write offset on the
+ * destination rank, or -offset-1 when that rank already appeared earlier in
+ * the token; the send path skips the payload of negative entries and sends
+ * only their 4-byte fp32 weight; the receiver copies the one row it got to the
+ * other expert rows locally).  Pass 1 writes x[r][s] to the destination row of
+ * every non-negative entry and every entry's gate to recv_weight at its row;
+ * pass 2 copies, on each receiving rank, the row of the token's first entry
+ * for that rank to the rows of its negative entries.  The final recv equals
+ * moonep_dispatch's.  Uses the route table built by moonep_plan.
+ * x : bf16 [R][S][H].  gates : fp32 [R][S][K].  recv : bf16 [R][C][H].
+ * recv_weight : fp32 [R][C] (the weight that arrived with each row).
+ * Requires K <= 128 (MOONEP_ERR_SHAPE otherwise). */
+int moonep_dispatch_send_once(const moonep_dims* dims, void* plan_ws, const uint16_t* x,
+                              const float* gates, uint16_t* recv, float* recv_weight,
+                              void* stream);
+
 /* Grouped GEMM over the [E+B, H, Hp] weight rows ("Moonshot AI 开源 MoonEP",
  * contract paragraph: the grouped GEMM addresses experts only by row index,
  * cu_seqlens chooses the active rows).  For each rank u and group g, rows
@@ -188,6 +211,16 @@ const char* moonep_status_string(int status);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t moonep_launch_count(void);
+
+/* Self-test of the device-side bounded wait used by the GEMM pipeline (no
+ * counterpart on the pages; failure-detection support).  Launches one tiny
+ * kernel that waits on an mbarrier nothing ever arrives on, with the GEMM's
+ * wait helper and a limit of limit_us microseconds (1 .. 1,000,000); when the
+ * limit expires it ORs MOONEP_ERR_TIMEOUT into *dev_status, writes the time it
+ * waited to *dev_elapsed_us and returns, leaving the context usable.
+ * dev_status, dev_elapsed_us : int32 device words (4-byte aligned). */
+int moonep_selftest_bounded_wait(int32_t* dev_status, uint32_t limit_us, int32_t* dev_elapsed_us,
+                                 void* stream);
 
 /* moonep_plan for callers that cannot allocate device memory.
  *

@@ -270,3 +270,47 @@ def full_plan(idx: np.ndarray, d: Dims) -> dict:
                 n_fills=nf, fills=fills, keep=p.keep, slot_expert=p.slot_expert,
                 n_recv=p.n_recv, src=p.src, cu_seqlens=p.cu_seqlens, dst=dst,
                 inverse=inverse)
+
+
+# ----------------------------------------------------------------------------
+# Send-once route encoding (Kimi K3 模型结构（8）, section 在线规划、零拷贝、静态 shape:
+# each route entry stores its write offset on the destination rank; an entry
+# whose destination rank already appeared earlier in the same token stores
+# -(offset) - 1, so the payload is sent once per (token, destination rank) and
+# copied locally on the receiver, while the fp32 weight is always sent).
+# Reading: "earlier" means a smaller k within the token.
+# ----------------------------------------------------------------------------
+
+def route_encoding(dst: np.ndarray, d: Dims) -> np.ndarray:
+    """route[r,s,k] = offset, or -offset-1 if the token already used that rank."""
+    flat = dst.reshape(d.R * d.S, d.K)
+    out = np.empty_like(flat)
+    for t in range(flat.shape[0]):
+        seen = set()
+        for k in range(d.K):
+            u, off = int(flat[t, k]) // d.C, int(flat[t, k]) % d.C
+            out[t, k] = -off - 1 if u in seen else off
+            seen.add(u)
+    return out.reshape(d.R, d.S, d.K)
+
+
+def link_traffic(dst: np.ndarray, d: Dims, payload_bytes: int, weight_bytes: int = 4) -> dict:
+    """Bytes that leave a token's own rank: once per entry (every entry carries
+    its payload) versus send-once (payload once per destination rank, weight
+    for every entry).  Entries whose destination is the token's own rank move
+    nothing across ranks."""
+    flat = dst.reshape(d.R, d.S, d.K)
+    remote_entries = 0
+    remote_pairs = 0
+    for r in range(d.R):
+        for s in range(d.S):
+            ranks = [int(v) // d.C for v in flat[r, s]]
+            remote = [u for u in ranks if u != r]
+            remote_entries += len(remote)
+            remote_pairs += len(set(remote))
+    return {
+        "remote_entries": remote_entries,
+        "remote_pairs": remote_pairs,
+        "per_entry_bytes": remote_entries * (payload_bytes + weight_bytes),
+        "send_once_bytes": remote_pairs * payload_bytes + remote_entries * weight_bytes,
+    }

@@ -20,6 +20,7 @@ OK = 0
 ERR_ARG, ERR_ALIGN, ERR_SLOTS, ERR_SHAPE, ERR_CUDA, ERR_SCRATCH = 1, 2, 3, 4, 5, 6
 ERR_ROUTING, ERR_INTERNAL, ERR_TIMEOUT = 0x100, 0x200, 0x400
 CNT_FILLS, CNT_MTILES, CNT_OCCUPIED, CNT_REDUCE = 0, 1, 2, 3
+CNT_REMOTE_ENTRIES, CNT_REMOTE_PAIRS = 4, 5
 
 
 class MoonepError(RuntimeError):
@@ -44,14 +45,15 @@ class moonep_dims(ctypes.Structure):
         return self.R * self.S * self.K
 
 
-_LAYOUT_FIELDS = ("total_bytes", "status", "counters", "counts", "T", "load", "keep", "gidx",
-                  "fills", "slot_expert", "n_recv", "src", "cu_seqlens", "dst", "inverse",
-                  "pieces", "occupied", "reduce", "mtiles")
+_SIZE_FIELDS = ("total_bytes", "status", "counters", "counts", "T", "load", "keep", "gidx",
+                "fills", "slot_expert", "n_recv", "src", "cu_seqlens", "dst", "inverse",
+                "pieces", "occupied", "reduce", "mtiles")
+_LAYOUT_FIELDS = _SIZE_FIELDS + ("route",)  # total size, then every table offset
 
 
 class moonep_plan_layout(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in _LAYOUT_FIELDS] + [
-        ("nchunk", ctypes.c_int32), ("max_mtiles", ctypes.c_int32)]
+    _fields_ = [(n, ctypes.c_size_t) for n in _SIZE_FIELDS] + [
+        ("nchunk", ctypes.c_int32), ("max_mtiles", ctypes.c_int32), ("route", ctypes.c_size_t)]
 
 
 _lib = None
@@ -73,6 +75,7 @@ def library() -> ctypes.CDLL:
         "moonep_plan": [D, P, P, P],
         "moonep_prefetch_weights": [D, P, P, P, P],
         "moonep_dispatch": [D, P, P, P, P],
+        "moonep_dispatch_send_once": [D, P, P, P, P, P, P],
         "moonep_grouped_gemm": [D, P, P, P, P, P, P],
         "moonep_combine": [D, P, P, P, P, P],
         "moonep_reduce_grad": [D, P, P, P, P],
@@ -86,6 +89,8 @@ def library() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.moonep_status_string.argtypes = [ctypes.c_int]
     lib.moonep_status_string.restype = ctypes.c_char_p
+    lib.moonep_selftest_bounded_wait.argtypes = [P, ctypes.c_uint32, P, P]
+    lib.moonep_selftest_bounded_wait.restype = ctypes.c_int
     lib.moonep_launch_count.argtypes = []
     lib.moonep_launch_count.restype = ctypes.c_uint64
     _lib = lib
@@ -177,6 +182,14 @@ def moonep_dispatch(d, plan_ws, x, recv, stream=None):
         _ptr(recv, torch.bfloat16, d.N * d.H, "recv"), _stream(stream)), "moonep_dispatch")
 
 
+def moonep_dispatch_send_once(d, plan_ws, x, gates, recv, recv_weight, stream=None):
+    _check(library().moonep_dispatch_send_once(
+        ctypes.byref(d), _ws(d, plan_ws), _ptr(x, torch.bfloat16, d.R * d.S * d.H, "x"),
+        _ptr(gates, torch.float32, d.N, "gates"), _ptr(recv, torch.bfloat16, d.N * d.H, "recv"),
+        _ptr(recv_weight, torch.float32, d.N, "recv_weight"), _stream(stream)),
+        "moonep_dispatch_send_once")
+
+
 def moonep_grouped_gemm(d, plan_ws, recv, w_home, w_slot, y, stream=None):
     hh = d.H * d.Hp
     _check(library().moonep_grouped_gemm(
@@ -206,6 +219,13 @@ def moonep_read_status(d, plan_ws, stream=None) -> int:
     _check(library().moonep_read_status(ctypes.byref(d), _ws(d, plan_ws), ctypes.byref(st),
                                         _stream(stream)), "moonep_read_status")
     return st.value
+
+
+def moonep_selftest_bounded_wait(dev_status, limit_us: int, dev_elapsed_us, stream=None):
+    _check(library().moonep_selftest_bounded_wait(
+        _ptr(dev_status, torch.int32, 1, "dev_status"), ctypes.c_uint32(limit_us),
+        _ptr(dev_elapsed_us, torch.int32, 1, "dev_elapsed_us"), _stream(stream)),
+        "moonep_selftest_bounded_wait")
 
 
 def moonep_launch_count() -> int:
@@ -244,5 +264,6 @@ class PlanWorkspace:
             "cu_seqlens": self.view("cu_seqlens", (d.R, d.E + d.B + 1)),
             "dst": self.view("dst", (d.R, d.S, d.K)),
             "inverse": self.view("inverse", (d.N,)),
+            "route": self.view("route", (d.R, d.S, d.K)),
         }
         return {k: t.cpu().numpy() for k, t in v.items()}

@@ -10,7 +10,8 @@ namespace moonep {
 
 constexpr int kMaxExperts = 4096;   // smem histograms hold E counters per warp
 constexpr int kChunkCopies = 4096;  // copies per histogram chunk (rounded to tokens)
-constexpr int kTileM = 128;         // GEMM rows per tile (one tcgen05 M=128 tile)
+constexpr int kTileM = 256;         // rows per GEMM work tile: two M=128 MMA accumulators
+constexpr int kMmaM = 128;          // rows of one tcgen05.mma (cta_group::1)
 constexpr int kHistWarps = 8;
 
 // Per-expert migrated range of global ordinals [lo, hi) and where it goes.
@@ -18,7 +19,7 @@ struct Piece {
   int32_t lo, hi, u, g;
 };
 
-// One 128-row GEMM tile: recv/y row of its first row, valid rows, the weight
+// One GEMM work tile of up to kTileM rows: recv/y row of its first row, valid rows, the weight
 // it multiplies (>= 0: home expert id; < 0: -1 - slot id u*B+j) and its rank.
 struct MTile {
   int32_t row0, rows, wsel, u;
@@ -40,6 +41,7 @@ struct PlanPtrs {
   int32_t* cu;
   int32_t* dst;
   int32_t* inverse;
+  int32_t* route;       // [R][S][K] send-once route entries
   Piece* pieces;        // [E][R]
   int32_t* piece_n;     // [E]
   int32_t* piece_base;  // [E][R] row_base = u*C + cu[u][g] - lo

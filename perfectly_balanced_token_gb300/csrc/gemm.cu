@@ -8,16 +8,23 @@
 //
 // Design (sm_103a):
 //  * persistent CTAs, one per SM; the work list is the planner's list of
-//    128-row tiles (device memory), times H'/BN column tiles.  Column tiles of
-//    one row tile are adjacent in the order, so concurrently running CTAs share
-//    the A tile and all tiles of one group share the expert's weights in L2.
-//  * warp 0: TMA producer (A box 64x128 K-major, B boxes 64x64 N-major, both
+//    work tiles of up to 256 rows of one group (device memory), times H'/BN
+//    column tiles.  Column tiles of one row tile are adjacent in the order, so
+//    concurrently running CTAs share the A rows and all tiles of one group
+//    share the expert's weights in L2.
+//  * a work tile is two 128-row halves that share every B stage: two
+//    128 x BN fp32 accumulators in TMEM (2*BN columns).  Per 64-deep K block a
+//    stage holds 2 A boxes and one B panel, so each byte of B fetched from L2
+//    feeds twice the MMA work of a single 128-row tile.  A tile whose group
+//    ends within its first half issues only the first half's MMAs.
+//  * warp 0: TMA producer (A boxes 64x128 K-major, B boxes 64x64 N-major, all
 //    128-byte swizzled) into a STAGES-deep shared-memory ring;
 //    warp 1: TMEM allocation and the single-thread tcgen05.mma issuer
 //    (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM);
-//    warps 2..5: epilogue, tcgen05.ld of the accumulator, bf16 rounding
-//    (nearest even), masked row stores.  The TMEM accumulator is double
-//    buffered so the epilogue of one tile overlaps the main loop of the next.
+//    warps 2..5: epilogue, tcgen05.ld of an accumulator, bf16 rounding
+//    (nearest even), masked row stores.  Each accumulator is released as soon
+//    as it is drained, so the next tile's first-half MMAs overlap the drain of
+//    the second half.
 //  * every mbarrier wait is bounded by the global timer; on expiry the kernel
 //    records MOONEP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and
 //    returns.
@@ -33,13 +40,20 @@ constexpr int kBK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle ro
 constexpr int kUmmaK = 16;     // K of one tcgen05.mma for 16-bit inputs
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitNs = 4000000000ull;  // 4 s per barrier wait
+// L2 policy: an A (recv) box is dead once the CTAs on its column tiles have read
+// it, so it is loaded evict-first; Y is written with streaming stores; the
+// weight panels, reused by every row tile of their group, keep normal priority.
+constexpr bool kAEvictFirst = true;
+constexpr bool kBEvictLast = false;
+constexpr bool kYStreaming = true;
 
 template <int BN, int STAGES>
 struct GemmCfg {
-  static constexpr int kABytes = kTileM * kBK * 2;
+  static constexpr int kAHalf = kMmaM * kBK * 2;       // one 128-row A box
+  static constexpr int kABytes = 2 * kAHalf;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kTmemCols = 2 * BN;             // accumulators: cols [0,BN) and [BN,2BN)
   static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
   static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
 };
@@ -75,14 +89,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of parity `parity` to complete.  Gives up when the
-// abort flag is raised by another role or after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// abort flag is raised by another role or after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void fence_barrier_init() {
@@ -99,6 +114,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -188,9 +221,9 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  const uint32_t tfull = bar0 + 8u * (2 * STAGES);
+  auto tempty = [&](int h) { return bar0 + 8u * (2 * STAGES + 1 + h); };  // h = accumulator half
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
@@ -203,10 +236,9 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), 4);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty(0), 4);
+    mbar_init(tempty(1), 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -231,19 +263,35 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN;
+        const bool two = mt.rows > kMmaM;
         const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
         const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * d.H;
+        const uint32_t bytes = Cfg::kAHalf * (two ? 2 : 1) + Cfg::kBBytes;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_expect_tx(full(stage), Cfg::kStageBytes);
+          mbar_expect_tx(full(stage), bytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
-          tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
+          if (kAEvictFirst) {
+            tma_load_2d_hint(sa, &tm_a, full(stage), kb * kBK, mt.row0, pol_a);
+            if (two)
+              tma_load_2d_hint(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM, pol_a);
+          } else {
+            tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
+            if (two) tma_load_2d(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM);
+          }
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          for (int i = 0; i < BN / 64; ++i) {
+            if (kBEvictLast)
+              tma_load_2d_hint(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64,
+                               wrow + kb * kBK, pol_b);
+            else
+              tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -261,14 +309,15 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kTileM, BN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      constexpr uint32_t idesc = make_idesc(kMmaM, BN);
+      int stage = 0;
+      uint32_t phase = 0, item = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++item) {
+        const bool two = p.mtiles[t / NT].rows > kMmaM;
+        // accumulator h is free once the epilogue released it for the previous item
+        if (!mbar_wait(tempty(0), (item & 1u) ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -278,14 +327,25 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
             const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
-            umma_bf16(dtm, ad, bd, idesc, (kb | k) != 0);
+            umma_bf16(tmem_base, ad, bd, idesc, (kb | k) != 0);
+          }
+          if (two) {
+            if (kb == 0) {
+              if (!mbar_wait(tempty(1), (item & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              const uint64_t ad = sw128_desc(sa + Cfg::kAHalf + k * (kUmmaK * 2), 16, 1024);
+              const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+              umma_bf16(tmem_base + BN, ad, bd, idesc, (kb | k) != 0);
+            }
           }
           umma_commit(empty(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(tfull(acc));
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        umma_commit(tfull);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -297,12 +357,11 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;  // TMEM lanes 32q..32q+31 are this warp's rows
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    uint32_t item = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++item) {
       const MTile mt = p.mtiles[t / NT];
       const int n0 = (t % NT) * BN;
-      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      const bool ok = mbar_wait(tfull, item & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
           *abort_flag = 1;
@@ -311,32 +370,37 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
         break;
       }
       tc_fence_after();
-      const int row = q * 32 + lane;
-      const bool valid = row < mt.rows;
-      uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_x32(tbase + c * 32, r);
-        tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+      for (int h = 0; h < 2; ++h) {
+        if (h == 0 || mt.rows > kMmaM) {
+          const int row = h * kMmaM + q * 32 + lane;
+          const bool valid = row < mt.rows;
+          uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
+          const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * BN);
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_x32(tbase + c * 32, r);
+            tmem_ld_wait();
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
-            o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
-            o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
-            o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
-            dst[v] = o;
+              for (int v = 0; v < 4; ++v) {
+                uint4 o;
+                o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+                o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+                o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+                o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+                if (kYStreaming) __stcs(dst + v, o);
+                else dst[v] = o;
+              }
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(h));  // every item releases both halves
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -346,6 +410,30 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// ever arrives on, with the same helper the GEMM pipeline uses, and must give up
+// after limit_ns, record MOONEP_ERR_TIMEOUT and return.
+__global__ void k_wait_selftest(int32_t* status, uint64_t limit_ns, int32_t* elapsed_us) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    if (!mbar_wait(smem_u32(&bar), 0, nullptr, limit_ns)) set_error(status, MOONEP_ERR_TIMEOUT);
+    *elapsed_us = (int32_t)((global_ns() - t0) / 1000);
+  }
+}
+
+cudaError_t launch_wait_selftest(int32_t* status, uint32_t limit_us, int32_t* elapsed_us,
+                                 cudaStream_t st, int* launches) {
+  k_wait_selftest<<<1, 32, 0, st>>>(status, (uint64_t)limit_us * 1000ull, elapsed_us);
+  *launches += 1;
+  return cudaGetLastError();
 }
 
 // -- host side ------------------------------------------------------------------
@@ -401,7 +489,7 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
                                 const void* w_home, const void* w_slot, void* y, cudaStream_t st,
                                 int* launches) {
   CUtensorMap ta, twh, tws;
-  if (!encode_2d(&ta, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, kTileM)) return cudaErrorInvalidValue;
+  if (!encode_2d(&ta, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, kMmaM)) return cudaErrorInvalidValue;
   if (!encode_2d(&twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64)) return cudaErrorInvalidValue;
   const void* ws = (w_slot != nullptr && d.B > 0) ? w_slot : w_home;
   const uint64_t ws_rows = (w_slot != nullptr && d.B > 0) ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H;
@@ -413,9 +501,9 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
   const long long max_tiles = (long long)d.max_mtiles * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sms, std::max<long long>(1, max_tiles));
   cudaError_t e;
-  if (bn == 256) e = launch_ggemm_cfg<256, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else if (bn == 128) e = launch_ggemm_cfg<128, 6>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else e = launch_ggemm_cfg<64, 8>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  if (bn == 256) e = launch_ggemm_cfg<256, 3>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else if (bn == 128) e = launch_ggemm_cfg<128, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else e = launch_ggemm_cfg<64, 5>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
   if (e == cudaSuccess) *launches += 1;
   return e;
 }

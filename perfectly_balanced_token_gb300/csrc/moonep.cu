@@ -12,11 +12,14 @@ namespace moonep {
 cudaError_t launch_plan(const Dims&, const int32_t*, const PlanPtrs&, cudaStream_t, int*);
 cudaError_t launch_prefetch(const Dims&, const PlanPtrs&, const void*, void*, cudaStream_t, int*);
 cudaError_t launch_dispatch(const Dims&, const PlanPtrs&, const void*, void*, cudaStream_t, int*);
+cudaError_t launch_dispatch_send_once(const Dims&, const PlanPtrs&, const void*, const float*, void*,
+                                      float*, cudaStream_t, int*);
 cudaError_t launch_grouped_gemm(const Dims&, const PlanPtrs&, const void*, const void*, const void*,
                                 void*, cudaStream_t, int*);
 cudaError_t launch_combine(const Dims&, const PlanPtrs&, const void*, const float*, void*,
                            cudaStream_t, int*);
 cudaError_t launch_reduce(const Dims&, const PlanPtrs&, float*, float*, cudaStream_t, int*);
+cudaError_t launch_wait_selftest(int32_t*, uint32_t, int32_t*, cudaStream_t, int*);
 
 static std::atomic<uint64_t> g_launches{0};
 
@@ -73,6 +76,7 @@ static Layout make_layout(const Dims& d) {
   p.cu_seqlens = take(4 * R * (EB + 1));
   p.dst = take(4 * N);
   p.inverse = take(4 * N);
+  p.route = take(4 * N);
   p.pieces = L.pieces = take(sizeof(Piece) * E * R);
   L.piece_n = take(4 * E);
   L.piece_base = take(4 * E * R);
@@ -107,6 +111,7 @@ static PlanPtrs resolve(const Layout& L, void* ws) {
   q.cu = (int32_t*)(b + p.cu_seqlens);
   q.dst = (int32_t*)(b + p.dst);
   q.inverse = (int32_t*)(b + p.inverse);
+  q.route = (int32_t*)(b + p.route);
   q.pieces = (Piece*)(b + L.pieces);
   q.piece_n = (int32_t*)(b + L.piece_n);
   q.piece_base = (int32_t*)(b + L.piece_base);
@@ -197,6 +202,21 @@ int moonep_dispatch(const moonep_dims* dims, void* plan_ws, const uint16_t* x, u
   return finish(e, n);
 }
 
+int moonep_dispatch_send_once(const moonep_dims* dims, void* plan_ws, const uint16_t* x,
+                              const float* gates, uint16_t* recv, float* recv_weight,
+                              void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(x);
+  MOONEP_NEED(gates);
+  MOONEP_NEED(recv);
+  MOONEP_NEED(recv_weight);
+  if (d.K > 128) return MOONEP_ERR_SHAPE;  // one thread per route entry in the send pass
+  int n = 0;
+  const cudaError_t e = launch_dispatch_send_once(d, P, x, gates, recv, recv_weight,
+                                                  (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
+
 int moonep_grouped_gemm(const moonep_dims* dims, void* plan_ws, const uint16_t* recv,
                         const uint16_t* w_home, const uint16_t* w_slot, uint16_t* y,
                         void* stream) {
@@ -271,6 +291,18 @@ const char* moonep_status_string(int s) {
 }
 
 uint64_t moonep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moonep_selftest_bounded_wait(int32_t* dev_status, uint32_t limit_us, int32_t* dev_elapsed_us,
+                                 void* stream) {
+  if (dev_status == nullptr || dev_elapsed_us == nullptr) return MOONEP_ERR_ARG;
+  if (limit_us == 0 || limit_us > 1000000u) return MOONEP_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) || (reinterpret_cast<uintptr_t>(dev_elapsed_us) & 3u))
+    return MOONEP_ERR_ALIGN;
+  int n = 0;
+  const cudaError_t e = launch_wait_selftest(dev_status, limit_us, dev_elapsed_us,
+                                             (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
 
 }  // extern "C"
 

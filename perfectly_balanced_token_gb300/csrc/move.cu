@@ -80,6 +80,71 @@ k_dispatch(Dims d, PlanPtrs p, const uint4* __restrict__ x, uint4* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
+// send-once dispatch, two passes ("Kimi K3 模型结构（8）", section 在线规划、零拷贝、
+// 静态 shape): the send pass writes a token's payload once per destination rank
+// (entries with route >= 0) and every entry's fp32 weight; the receive pass
+// replicates, on the destination rank, the row that arrived to the rows of the
+// token's later entries for that rank (route < 0).
+// ---------------------------------------------------------------------------
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads)
+k_send(Dims d, PlanPtrs p, const uint4* __restrict__ x, const float* __restrict__ gates,
+       uint4* __restrict__ recv, float* __restrict__ recv_w) {
+  if (plan_failed(p.status)) return;
+  const int hv = d.H / 8;
+  const int ntok = d.R * d.S;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    const int32_t* rt = p.route + (size_t)t * d.K;
+    if (threadIdx.x < d.K) {  // weights travel with every entry
+      const int k = threadIdx.x;
+      recv_w[__ldg(dt + k)] = __ldg(gates + (size_t)t * d.K + k);
+    }
+    const uint4* xr = x + (size_t)t * hv;
+    uint4 v[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int a = threadIdx.x + i * kRowThreads;
+      if (a < hv) v[i] = __ldcs(xr + a);
+    }
+    for (int k = 0; k < d.K; ++k) {
+      const int code = __ldg(rt + k);
+      if (code < 0) continue;  // payload already sent to that rank
+      const int u = __ldg(dt + k) / d.C;
+      uint4* out = recv + ((size_t)u * d.C + code) * hv;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int a = threadIdx.x + i * kRowThreads;
+        if (a < hv) __stcs(out + a, v[i]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+k_receive_copy(Dims d, PlanPtrs p, uint4* __restrict__ recv) {
+  if (plan_failed(p.status)) return;
+  const int hv = d.H / 8;
+  const int ntok = d.R * d.S;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    const int32_t* rt = p.route + (size_t)t * d.K;
+    for (int k = 1; k < d.K; ++k) {
+      const int code = __ldg(rt + k);
+      if (code >= 0) continue;
+      const int u = __ldg(dt + k) / d.C;
+      int first = -1;  // the entry of this token that carried the payload to u
+      for (int j = 0; j < k && first < 0; ++j)
+        if (__ldg(rt + j) >= 0 && __ldg(dt + j) / d.C == u) first = __ldg(rt + j);
+      if (first < 0) continue;  // cannot happen for a plan-built route table
+      const uint4* src = recv + ((size_t)u * d.C + first) * hv;
+      uint4* dst = recv + ((size_t)u * d.C + (-code - 1)) * hv;
+      for (int a = threadIdx.x; a < hv; a += kRowThreads) dst[a] = src[a];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // combine: out[r,s] = bf16( sum_k gates[r,s,k] * y[dst[r,s,k]] ), k ascending,
 // fp32 fused multiply-add ("Kimi K3 模型结构（8）", same section: each expert
 // output is scaled by its own fp32 router weight)
@@ -240,6 +305,27 @@ cudaError_t launch_dispatch(const Dims& d, const PlanPtrs& p, const void* x, voi
   else if (vpt <= 16) k_dispatch<16><<<grid, kRowThreads, 0, st>>>(d, p, xs, rv);
   else return cudaErrorInvalidValue;
   *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_send_once(const Dims& d, const PlanPtrs& p, const void* x,
+                                      const float* gates, void* recv, float* recv_w,
+                                      cudaStream_t st, int* launches) {
+  const int hv = d.H / 8;
+  const int vpt = (hv + kRowThreads - 1) / kRowThreads;
+  const int ntok = d.R * d.S;
+  const int grid = min(ntok, sm_count() * 16);
+  const uint4* xs = (const uint4*)x;
+  uint4* rv = (uint4*)recv;
+  if (d.K > kRowThreads) return cudaErrorInvalidValue;
+  if (vpt <= 1) k_send<1><<<grid, kRowThreads, 0, st>>>(d, p, xs, gates, rv, recv_w);
+  else if (vpt <= 2) k_send<2><<<grid, kRowThreads, 0, st>>>(d, p, xs, gates, rv, recv_w);
+  else if (vpt <= 4) k_send<4><<<grid, kRowThreads, 0, st>>>(d, p, xs, gates, rv, recv_w);
+  else if (vpt <= 8) k_send<8><<<grid, kRowThreads, 0, st>>>(d, p, xs, gates, rv, recv_w);
+  else if (vpt <= 16) k_send<16><<<grid, kRowThreads, 0, st>>>(d, p, xs, gates, rv, recv_w);
+  else return cudaErrorInvalidValue;
+  k_receive_copy<<<grid, kRowThreads, 0, st>>>(d, p, rv);
+  *launches += 2;
   return cudaGetLastError();
 }
 

@@ -102,6 +102,7 @@ k_plan(Dims d, PlanPtrs p) {
   int32_t* sState = sLoad + d.R;    // [R]
   int32_t* sCur = sState + d.R;     // [R]
   int32_t* sTiles = sCur + d.R;     // [R]
+  int32_t* sPieceN = sTiles + d.R;  // [E] pieces per expert so far
   if (plan_failed(p.status)) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int EB = d.E + d.B;
@@ -111,6 +112,7 @@ k_plan(Dims d, PlanPtrs p) {
   for (int e = tid; e < d.E; e += nt) {
     int run = 0;
     int32_t* c = p.counts + e;
+#pragma unroll 8
     for (int i = 0; i < rc; ++i) {
       const int v = c[(size_t)i * d.E];
       c[(size_t)i * d.E] = run;
@@ -119,7 +121,7 @@ k_plan(Dims d, PlanPtrs p) {
     sT[e] = run;
     p.T[e] = run;
     sMig[e] = 0;
-    p.piece_n[e] = 0;
+    sPieceN[e] = 0;
     p.red_n[e] = 0;
   }
   for (int s = tid; s < d.R * d.B; s += nt) p.slot_expert[s] = -1;
@@ -163,10 +165,10 @@ k_plan(Dims d, PlanPtrs p) {
         const int t = min(left, need);
         const int g = (j < d.B) ? d.E + j : e;  // slot, or inference overflow row
         if (j < d.B) p.slot_expert[u * d.B + j] = e;
-        const int pi = p.piece_n[e];
+        const int pi = sPieceN[e];
         if (pi >= d.R) { ok = false; break; }
         p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
-        p.piece_n[e] = pi + 1;
+        sPieceN[e] = pi + 1;
         p.cu[(size_t)u * (EB + 1) + g + 1] = t;
         sTiles[u] += (t + kTileM - 1) / kTileM;
         sMig[e] += t;
@@ -194,6 +196,7 @@ k_plan(Dims d, PlanPtrs p) {
 
   // keep, home rows, per-rank tile counts
   for (int e = tid; e < d.E; e += nt) {
+    p.piece_n[e] = sPieceN[e];
     const int k = sT[e] - sMig[e];
     p.keep[e] = k;
     const int h = e / d.L;
@@ -360,6 +363,46 @@ k_dst(Dims d, const int32_t* __restrict__ idx, PlanPtrs p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// 5. send-once route entries ("Kimi K3 模型结构（8）", section 在线规划、零拷贝、
+//    静态 shape): per token, entry k keeps its row offset on its destination
+//    rank unless an earlier entry of the token goes to the same rank, in which
+//    case it stores -offset-1.  Also counts the entries and the distinct
+//    (token, rank) pairs that leave the token's own rank.  One thread per token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+k_route(Dims d, PlanPtrs p) {
+  if (plan_failed(p.status)) return;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  int entries = 0, pairs = 0;
+  if (t < d.R * d.S) {
+    const int r = t / d.S;
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    int32_t* rt = p.route + (size_t)t * d.K;
+    for (int k = 0; k < d.K; ++k) {
+      const int v = dt[k];
+      const int u = v / d.C;
+      bool dup = false;
+      for (int j = 0; j < k; ++j) dup |= (dt[j] / d.C == u);
+      const int off = v - u * d.C;
+      rt[k] = dup ? -off - 1 : off;
+      if (u != r) {
+        ++entries;
+        pairs += dup ? 0 : 1;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    entries += __shfl_xor_sync(0xffffffffu, entries, o);
+    pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+  }
+  if ((threadIdx.x & 31) == 0 && (entries | pairs)) {
+    atomicAdd(&p.counters[MOONEP_CNT_REMOTE_ENTRIES], entries);
+    atomicAdd(&p.counters[MOONEP_CNT_REMOTE_PAIRS], pairs);
+  }
+}
+
 cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cudaStream_t st,
                         int* launches) {
   cudaError_t err = cudaMemsetAsync(p.status, 0, 256, st);  // status + counters header
@@ -370,7 +413,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     if (err != cudaSuccess) return err;
   }
   k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
-  const size_t plan_smem = sizeof(int32_t) * (2 * d.E + 4 * d.R);
+  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 4 * d.R);
   if (plan_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;
@@ -378,7 +421,8 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
   k_plan<<<1, 1024, plan_smem, st>>>(d, p);
   k_tables<<<d.R, 1024, 0, st>>>(d, p);
   k_dst<<<dim3(d.nchunk, d.R), 256, 0, st>>>(d, idx, p);
-  *launches += 4;
+  k_route<<<(d.R * d.S + 255) / 256, 256, 0, st>>>(d, p);
+  *launches += 5;
   return cudaGetLastError();
 }
 

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -88,6 +88,8 @@ def test_bad_pointers_rejected_before_launch(lib):
     assert lib.moonep_plan(D, ok, P(0x10008), None) == _lib.ERR_ALIGN
     assert lib.moonep_dispatch(D, ws, ok, None, None) == _lib.ERR_ARG
     assert lib.moonep_dispatch(D, ws, odd, ok, None) == _lib.ERR_ALIGN
+    assert lib.moonep_dispatch_send_once(D, ws, ok, ok, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_dispatch_send_once(D, ws, ok, odd, ok, ok, None) == _lib.ERR_ALIGN
     assert lib.moonep_prefetch_weights(D, ws, ok, None, None) == _lib.ERR_ARG
     assert lib.moonep_grouped_gemm(D, ws, ok, ok, None, ok, None) == _lib.ERR_ARG
     assert lib.moonep_grouped_gemm(D, ws, ok, odd, ok, ok, None) == _lib.ERR_ALIGN
@@ -109,6 +111,16 @@ def test_noalloc_planner_rejects_dims_beyond_its_scratch(lib):
                                  ctypes.c_void_p(0x10000), None)
     assert rc == _lib.ERR_SCRATCH
     assert "scratch" in mx.status_string(rc)
+    assert mx.moonep_launch_count() == n0
+
+
+def test_selftest_wait_rejects_bad_arguments(lib):
+    n0 = mx.moonep_launch_count()
+    P = ctypes.c_void_p
+    assert lib.moonep_selftest_bounded_wait(None, 1000, P(0x1000), None) == _lib.ERR_ARG
+    assert lib.moonep_selftest_bounded_wait(P(0x1000), 0, P(0x1004), None) == _lib.ERR_ARG
+    assert lib.moonep_selftest_bounded_wait(P(0x1000), 1000001, P(0x1004), None) == _lib.ERR_ARG
+    assert lib.moonep_selftest_bounded_wait(P(0x1002), 1000, P(0x1004), None) == _lib.ERR_ALIGN
     assert mx.moonep_launch_count() == n0
 
 

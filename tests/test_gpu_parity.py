@@ -179,3 +179,27 @@ def test_bad_routing_sets_status_and_writes_nothing(bad):
         assert bool((t.view(torch.int16) == 0x7F7F).all())
     if w.B:
         assert bool((run.w_slot.view(torch.int16) == 0x7F7F).all())
+
+
+@pytest.mark.parametrize("name,w,mk", CASES, ids=[c[0] for c in CASES])
+def test_send_once_route_and_dispatch(name, w, mk):
+    """Route entries and link counters bit-exact with the oracle's encoding;
+    the two-pass send-once dispatch fills recv exactly like the fused one and
+    delivers every entry's weight to its row."""
+    rt = mk(w)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt)
+    tabs = run.plan()
+    assert np.array_equal(tabs["route"], oplanner.route_encoding(fp["dst"], od))
+    traffic = oplanner.link_traffic(fp["dst"], od, payload_bytes=2 * w.H)
+    assert int(tabs["counters"][4]) == traffic["remote_entries"]
+    assert int(tabs["counters"][5]) == traffic["remote_pairs"]
+    recv_w = torch.full((w.N,), -1.0, dtype=torch.float32, device="cuda")
+    mx.moonep_dispatch_send_once(run.d, run.ws.buf, run.x, run.gates, run.recv, recv_w)
+    torch.cuda.synchronize()
+    want = olayer.permute(gh.host_bits(run.x), fp["dst"], od)
+    assert np.array_equal(gh.host_bits(run.recv).reshape(w.N, w.H), want)
+    got_w = recv_w.cpu().numpy()
+    assert np.array_equal(got_w[fp["dst"].reshape(-1)], rt.gates.reshape(-1))
+    run.check_all_guards()

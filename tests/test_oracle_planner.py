@@ -196,3 +196,46 @@ def test_generator_skew_agrees_with_oracle_maxvio():
     v = theory.maxvio(T, 8 * 1024 * 4, 64)
     assert v == pytest.approx(syn.input_skew(rt.idx, 64))
     assert abs(v - 1.0) <= 0.05
+
+
+def test_route_encoding_hand_case():
+    case = json.load(open(os.path.join(GOLD, "hand_plans.json")))["route_cases"][0]
+    R, S, K, C, owner = case["R"], case["S"], case["K"], case["C"], case["owner"]
+    d = Dims(R=R, E=R, B=1, K=K, S=S)
+    assert d.C == C
+    dst = np.zeros((R, S, K), dtype=np.int64)
+    for r in range(R):
+        for s in range(S):
+            dst[r, s] = r * C + s * K + np.arange(K)  # stays on its own rank
+    dst[owner, 0] = [u * C + o for u, o in zip(case["dst_rank"], case["offset"])]
+    enc = planner.route_encoding(dst, d)
+    assert enc[owner, 0].tolist() == case["route"]
+    # a token whose K entries share one rank carries its payload in entry 0 only
+    assert enc[owner, 1, 0] >= 0 and np.all(enc[owner, 1, 1:] < 0)
+    traffic = planner.link_traffic(dst, d, payload_bytes=7168)
+    assert traffic["remote_entries"] == case["remote_entries"]
+    assert traffic["remote_pairs"] == case["remote_pairs"]
+    assert traffic["send_once_bytes"] == 2 * 7168 + 5 * 4
+    assert traffic["per_entry_bytes"] == 5 * (7168 + 4)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_route_encoding_invariants(seed):
+    R, E, B, K, S = 8, 64, 8, 4, 256
+    d = Dims(R=R, E=E, B=B, K=K, S=S)
+    rt = syn.gumbel_topk_routing(R, S, K, E, alpha=1.0 + seed, seed=seed)
+    fp = planner.full_plan(rt.idx, d)
+    enc = planner.route_encoding(fp["dst"], d).reshape(-1, K)
+    dst = fp["dst"].reshape(-1, K)
+    for t in range(dst.shape[0]):
+        ranks = dst[t] // d.C
+        nonneg = enc[t] >= 0
+        # exactly one payload-carrying entry per distinct destination rank, the first
+        assert sorted(ranks[nonneg].tolist()) == sorted(set(ranks.tolist()))
+        assert nonneg[0]
+        # decoding recovers every offset
+        dec = np.where(enc[t] >= 0, enc[t], -enc[t] - 1)
+        assert np.array_equal(dec, dst[t] % d.C)
+    tr = planner.link_traffic(fp["dst"], d, payload_bytes=2 * 64)
+    assert tr["send_once_bytes"] <= tr["per_entry_bytes"]
+    assert tr["remote_pairs"] <= tr["remote_entries"]

@@ -21,7 +21,7 @@ from perfectly_balanced_token_gb300 import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 OUTPUT_TABLES = ("status", "counters", "T", "load", "keep", "gidx", "fills", "slot_expert",
-                 "n_recv", "src", "cu_seqlens", "dst", "inverse", "occupied", "reduce")
+                 "n_recv", "src", "cu_seqlens", "dst", "inverse", "route", "occupied", "reduce")
 
 
 @pytest.fixture(scope="module", autouse=True)
