@@ -41,8 +41,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 def _profile_workload():
     from perfectly_balanced_token_gb300 import synthetic as syn
-    # the pages shape's H, H', K with fewer experts and tokens: a few GB on the device
+    # the pages shape's H, H', K with fewer experts and tokens: a few GB on the
+    # device; C*R/E = 4096 rows per group, so the GEMM runs 256-row work tiles
     return syn.Workload("profile-sized", R=8, E=16, B=2, K=8, S=1024, H=7168, Hp=2048)
+
+
+def _profile128_workload():
+    from perfectly_balanced_token_gb300 import synthetic as syn
+    # as above with E=24: C*R/E = 2731 rows per group, so 128-row work tiles
+    # (the GEMM variant the pages shape uses)
+    return syn.Workload("profile-sized-128", R=8, E=24, B=3, K=8, S=1024, H=7168, Hp=2048)
 
 
 def _pages():
@@ -55,8 +63,9 @@ def _k3():
     return syn.K3
 
 
-WORKLOADS = {"pages": _pages, "k3": _k3, "profile": _profile_workload}
-DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,)}
+WORKLOADS = {"pages": _pages, "k3": _k3, "profile": _profile_workload,
+             "profile128": _profile128_workload}
+DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,), "profile128": (1.0,)}
 
 
 def load_peaks():
@@ -179,7 +188,6 @@ def run_ours(args):
 
     w = WORKLOADS[args.workload]()
     sweep = tuple(args.maxvio) if args.maxvio else DEFAULT_SWEEP.get(args.workload, SWEEP)
-    d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode)
     N = w.N
     st = torch.cuda.current_stream()
 
@@ -196,106 +204,130 @@ def run_ours(args):
     g_home = syn.normal_f32((w.E, w.H, w.Hp), 1.0, 3, dev)
     g_slot = syn.normal_f32((w.R, w.B, w.H, w.Hp), 1.0, 4, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    ws = mx.PlanWorkspace(d, device=dev)
     names = ("plan", "prefetch", "dispatch", "gemm", "combine", "reduce_grad")
-
-    def calls(j):
-        # stream=None: the current stream (the capture stream while capturing)
-        return (
-            lambda: mx.moonep_plan(d, idx[j], ws.buf),
-            lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot),
-            lambda: mx.moonep_dispatch(d, ws.buf, x, recv),
-            lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y),
-            lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out),
-            lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot),
-        )
-
     clocks = ClockSampler(local)
     clocks.start()  # before the warm-up, so nvidia-smi's start-up is over by the timed region
-    for i in range(args.warmup):
-        for c in calls(i % len(sweep)):
-            c()
-    torch.cuda.synchronize()
-    status = mx.moonep_read_status(d, ws.buf)
-    if status:
-        raise RuntimeError(f"device status {status:#x}: {mx.status_string(status)}")
 
-    # per-maxvio plan counters (outside the timed region)
-    counters = []
-    for j in range(len(sweep)):
-        mx.moonep_plan(d, idx[j], ws.buf, st)
-        c = ws.view("counters", (8,)).cpu().tolist()
-        counters.append({"fills": c[0], "mtiles": c[1], "occupied_slots": c[2],
-                         "reduced_experts": c[3]})
+    def time_policy(policy, warmup, steps):
+        """Warm up eagerly, capture one CUDA graph per (routing, segment), then
+        time `steps` steps of graph replays with events between segments."""
+        d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy)
+        ws = mx.PlanWorkspace(d, device=dev)
 
-    # one CUDA graph per (routing, segment): the timed loop only replays graphs, so
-    # host-side enqueue cost never shows up between the per-segment events
-    graphs, graph_launches = [], []
-    for j in range(len(sweep)):
-        gj, lj = [], []
-        for c in calls(j):
-            g = torch.cuda.CUDAGraph()
-            n0 = mx.moonep_launch_count()
-            with torch.cuda.graph(g):
+        def calls(j):
+            # stream=None: the current stream (the capture stream while capturing)
+            return (
+                lambda: mx.moonep_plan(d, idx[j], ws.buf),
+                lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot),
+                lambda: mx.moonep_dispatch(d, ws.buf, x, recv),
+                lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y),
+                lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out),
+                lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot),
+            )
+
+        for i in range(warmup):
+            for c in calls(i % len(sweep)):
                 c()
-            lj.append(mx.moonep_launch_count() - n0)
-            gj.append(g)
-        graphs.append(gj)
-        graph_launches.append(lj)
-    for j in range(len(sweep)):  # first replay uploads each graph
-        for g in graphs[j]:
-            g.replay()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        status = mx.moonep_read_status(d, ws.buf)
+        if status:
+            raise RuntimeError(f"device status {status:#x}: {mx.status_string(status)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches = 0
-    t_wall0 = time.perf_counter()
-    t_epoch0 = time.time()
-    for i in range(args.steps):
-        j = i % len(sweep)
-        flush.fill_(float(i))  # evict L2 between steps (not inside a step's events)
-        for k in range(6):
-            evs[i][k].record()
-            graphs[j][k].replay()
-        evs[i][6].record()
-        launches += sum(graph_launches[j])
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    t_epoch1 = time.time()
-    if world > 1:
-        dist.barrier()
-    status = mx.moonep_read_status(d, ws.buf)
-    if status:
-        raise RuntimeError(f"device status after the timed steps {status:#x}: "
-                           f"{mx.status_string(status)}")
+        counters = []  # per-maxvio plan counters (outside the timed region)
+        for j in range(len(sweep)):
+            mx.moonep_plan(d, idx[j], ws.buf, st)
+            c = ws.view("counters", (8,)).cpu().tolist()
+            n_recv = ws.view("n_recv", (w.R,)).cpu()
+            payload = 2 * w.H
+            counters.append({"fills": c[0], "mtiles": c[1], "occupied_slots": c[2],
+                             "reduced_experts": c[3], "max_redundant_per_rank": int(n_recv.max()),
+                             "link_bytes_per_entry": c[4] * (payload + 4),
+                             "link_bytes_send_once": c[5] * payload + c[4] * 4})
 
-    seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(6)]
-                    for i in range(args.steps)])  # ms
+        # the timed loop only replays graphs, so host-side enqueue cost never
+        # shows up between the per-segment events
+        graphs, graph_launches = [], []
+        for j in range(len(sweep)):
+            gj, lj = [], []
+            for c in calls(j):
+                g = torch.cuda.CUDAGraph()
+                n0 = mx.moonep_launch_count()
+                with torch.cuda.graph(g):
+                    c()
+                lj.append(mx.moonep_launch_count() - n0)
+                gj.append(g)
+            graphs.append(gj)
+            graph_launches.append(lj)
+        for j in range(len(sweep)):  # first replay uploads each graph
+            for g in graphs[j]:
+                g.replay()
+        torch.cuda.synchronize()
+
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        launches = 0
+        t0 = time.time()
+        for i in range(steps):
+            j = i % len(sweep)
+            flush.fill_(float(i))  # evict L2 between steps (not inside a step's events)
+            for k in range(6):
+                evs[i][k].record()
+                graphs[j][k].replay()
+            evs[i][6].record()
+            launches += sum(graph_launches[j])
+        torch.cuda.synchronize()
+        t1 = time.time()
+        if world > 1:
+            dist.barrier()
+        status = mx.moonep_read_status(d, ws.buf)
+        if status:
+            raise RuntimeError(f"device status after the timed steps {status:#x}: "
+                               f"{mx.status_string(status)}")
+        seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(6)]
+                        for i in range(steps)])  # ms
+        return d, ws, seg, counters, launches, (t0, t1)
+
+    headline_rows = [0, 2, 3, 4]
+
+    def per_maxvio(seg_, counters_):
+        out_ = []
+        sm = seg_.sum(axis=1)
+        for j, mv in enumerate(sweep):
+            rows = [i for i in range(seg_.shape[0]) if i % len(sweep) == j]
+            if not rows:
+                continue
+            ms = float(sm[rows].mean())
+            hl = float(seg_[rows][:, headline_rows].sum(axis=1).mean())
+            out_.append({"maxvio_target": mv, "maxvio": round(measured_mv[j], 4),
+                         "value": N / (ms / 1e3), "ms_per_step": ms,
+                         "value_plan_permute_gemm_combine": N / (hl / 1e3),
+                         "breakdown_ms": {n: float(seg_[rows][:, k].mean())
+                                          for k, n in enumerate(names)},
+                         **counters_[j]})
+        return out_
+
+    d, ws, seg, counters, launches, window = time_policy(0, args.warmup, args.steps)
     step_ms = seg.sum(axis=1)
     total_ms = reduce_max(float(step_ms.sum()), world, dev)
-    headline_rows = [0, 2, 3, 4]
-    per_mv = []
-    for j, mv in enumerate(sweep):
-        rows = [i for i in range(args.steps) if i % len(sweep) == j]
-        if not rows:
-            continue
-        ms = float(step_ms[rows].mean())
-        hl = float(seg[rows][:, headline_rows].sum(axis=1).mean())
-        per_mv.append({"maxvio_target": mv, "maxvio": round(measured_mv[j], 4),
-                       "value": N / (ms / 1e3), "ms_per_step": ms,
-                       "value_plan_permute_gemm_combine": N / (hl / 1e3),
-                       "breakdown_ms": {n: float(seg[rows][:, k].mean()) for k, n in enumerate(names)},
-                       **counters[j]})
+    t_wall = window[1] - window[0]
+    per_mv = per_maxvio(seg, counters)
+    policy1 = None
+    if not args.no_policy_sweep:
+        _, _, seg1, counters1, _, _ = time_policy(1, 1, args.steps)
+        ms1 = reduce_max(float(seg1.sum()), world, dev)
+        policy1 = {"planner": "largest first (dims.policy = 1)",
+                   "value": N * args.steps * world / (ms1 / 1e3),
+                   "ms_per_step": ms1 / args.steps,
+                   "sweep": per_maxvio(seg1, counters1)}
 
     # e2e: host buffers through the same C ABI, copies inside the timed region
     e2e = None if args.no_e2e else run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot,
                                             g_home, g_slot, dev, st, world)
     clocks.stop()
-    clk = clocks.summary(t_epoch0, t_epoch1)
+    clk = clocks.summary(*window)
 
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -339,6 +371,8 @@ def run_ours(args):
         "wall_s_timed_region": t_wall, "timing": "CUDA events between CUDA-graph replays of each "
         "segment on the launching stream; gpu_launches counted from the captured graphs",
         "step_ms": [float(v) for v in step_ms],
+        "planner": "Theorem 1 construction, fixed tie-break (dims.policy = 0)",
+        "planner_largest_first": policy1,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "pages":
         result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
@@ -492,6 +526,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-policy-sweep", action="store_true",
+                    help="skip timing the largest-first planner policy")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pages",
                     help="pages = the headline configuration; the others are smaller cases "
                          "of the same kernels for profiling")

@@ -45,12 +45,19 @@ extern "C" {
 
 typedef struct moonep_dims {
   int32_t R, E, B, K, S, H, Hp;
-  int32_t mode; /* 0 = training (requires B >= E/R), 1 = inference (B >= 0) */
+  int32_t mode;   /* 0 = training (requires B >= E/R), 1 = inference (B >= 0) */
+  int32_t policy; /* planner choice among the plans Theorem 1 allows:
+                     0 = the smallest-id underloaded rank from the smallest-id
+                         overloaded rank, donor experts in descending id;
+                     1 = largest first: the rank with the largest deficit from
+                         the rank with the largest surplus, donor experts in
+                         descending remaining copies (fewest distinct experts
+                         per fill) */
 } moonep_dims;
 
 enum moonep_status {
   MOONEP_OK = 0,
-  MOONEP_ERR_ARG = 1,      /* null pointer, non-positive dimension, bad mode   */
+  MOONEP_ERR_ARG = 1,      /* null pointer, non-positive dimension, bad mode or policy */
   MOONEP_ERR_ALIGN = 2,    /* a pointer is not 16-byte aligned                 */
   MOONEP_ERR_SLOTS = 3,    /* training mode with B < E/R                       */
   MOONEP_ERR_SHAPE = 4,    /* E % R != 0, K > E, E > 4096, H or Hp not a multiple
@@ -85,7 +92,7 @@ typedef struct moonep_plan_layout {
   size_t pieces;       /* internal: per-expert ranges of ordinals and their rows */
   size_t occupied;     /* int32[R*B] occupied slot ids u*B+j, ascending          */
   size_t reduce;       /* internal: per-expert slot lists for reduce_grad        */
-  size_t mtiles;       /* internal: 256-row GEMM work tiles (int32[4] each)      */
+  size_t mtiles;       /* internal: GEMM work tiles of 128 or 256 rows (int32[4]) */
   int32_t nchunk;      /* token chunks per rank used by the histogram            */
   int32_t max_mtiles;
   size_t route;        /* int32[R][S][K] send-once route entries: the copy's row
@@ -96,7 +103,7 @@ typedef struct moonep_plan_layout {
 /* Index of each counter in the `counters` table. */
 enum moonep_counter {
   MOONEP_CNT_FILLS = 0,    /* fills performed (<= R-1)                     */
-  MOONEP_CNT_MTILES = 1,   /* 256-row GEMM work tiles over all ranks and groups */
+  MOONEP_CNT_MTILES = 1,   /* GEMM work tiles over all ranks and groups    */
   MOONEP_CNT_OCCUPIED = 2, /* occupied prefetch slots                      */
   MOONEP_CNT_REDUCE = 3,   /* home experts with at least one slot copy     */
   MOONEP_CNT_REMOTE_ENTRIES = 4, /* route entries whose destination is not the token's own rank */
@@ -116,10 +123,11 @@ int moonep_get_plan_layout(const moonep_dims* dims, moonep_plan_layout* out);
  * ("Kimi K3 模型结构（8）：训练并行，MoonEP 与四类等待", section 定理 1; "MoonEP :
  * l'équilibrage parfait", section Le théorème): ranks with fewer than C copies
  * on their home experts are underloaded, those with more are overloaded; the
- * smallest-id underloaded rank u is filled to exactly C from the smallest-id
- * overloaded rank o, taking o's local experts in descending id and, inside an
- * expert, the copies with the highest ordinal first; o goes back to the set
- * matching its new load; at most R-1 fills.  Then the buffer layout of the
+ * underloaded rank u is filled to exactly C from one overloaded rank o (which
+ * pair and which of o's experts: dims->policy), taking inside an expert the
+ * copies with the highest ordinal first; o goes back to the set matching its
+ * new load; at most R-1 fills and at most E/R experts per receiving rank
+ * whatever the policy.  Then the buffer layout of the
  * framework contract ("Moonshot AI 开源 MoonEP", contract paragraph): rank u's
  * C rows are grouped by weight row g in [0, E+B) ascending (rows [0,E) home
  * experts, [E, E+B) slots), copies in ascending ordinal inside a group,

@@ -55,7 +55,8 @@ class Dims:
     S: int
     H: int = 0
     Hp: int = 0
-    mode: int = 0  # 0 training, 1 inference
+    mode: int = 0    # 0 training, 1 inference
+    policy: int = 0  # 0 constructive tie-break, 1 largest first
 
     @property
     def L(self) -> int:
@@ -135,7 +136,19 @@ class Plan:
 
 
 def constructive_plan(T: np.ndarray, d: Dims) -> tuple[list, np.ndarray]:
-    """Theorem 1's construction with the fixed tie-break.
+    """Theorem 1's construction with a fixed tie-break.
+
+    policy 0 (the proof's plain order): the smallest-id underloaded rank u is
+    filled from the smallest-id overloaded rank o, taking o's experts in
+    descending expert id.
+    policy 1 (largest first): u is the underloaded rank with the largest
+    deficit C - load, o the overloaded rank with the largest surplus
+    load - C (ties: smallest id), and o's experts are taken in descending
+    order of their remaining copies (ties: descending id).  Taking the largest
+    remaining experts first covers a fill with the fewest distinct experts.
+    Both: inside an expert the copies with the highest global ordinals move.
+    The proof's bounds (at most R-1 fills, at most E/R experts per receiving
+    rank) hold for any choice of u, o and copies.
 
     Returns the fills (each with the expert ranges it moved) and, per expert,
     how many of its copies were migrated away from the home rank.
@@ -144,21 +157,30 @@ def constructive_plan(T: np.ndarray, d: Dims) -> tuple[list, np.ndarray]:
     load = [int(x) for x in np.asarray(T).reshape(d.R, L).sum(axis=1)]
     under = sorted(h for h in range(d.R) if load[h] < C)
     over = sorted(h for h in range(d.R) if load[h] > C)
-    cursor = {h: (h + 1) * L - 1 for h in over}   # next expert to draw from
+    cursor = {h: (h + 1) * L - 1 for h in over}   # next expert to draw from (policy 0)
     migrated = [0] * d.E
     fills = []
     while under:
-        u, o = under[0], over[0]
+        if d.policy == 1:
+            u = min(under, key=lambda h: (load[h] - C, h))   # largest deficit
+            o = max(over, key=lambda h: (load[h] - C, -h))   # largest surplus
+        else:
+            u, o = under[0], over[0]
         f = Fill(u=u, o=o, d=C - load[u])
         need = f.d
         while need > 0:
-            e = cursor[o]
-            left = int(T[e]) - migrated[e]
-            if left == 0:
-                cursor[o] = e - 1
-                # o is overloaded, so its own unmigrated copies exceed `need`
-                assert cursor[o] >= o * L, "overloaded rank ran out of copies"
-                continue
+            if d.policy == 1:
+                cand = [(int(T[e]) - migrated[e], e) for e in range(o * L, (o + 1) * L)]
+                left, e = max(cand)  # most remaining copies, then highest id
+                assert left > 0, "overloaded rank ran out of copies"
+            else:
+                e = cursor[o]
+                left = int(T[e]) - migrated[e]
+                if left == 0:
+                    cursor[o] = e - 1
+                    # o is overloaded, so its own unmigrated copies exceed `need`
+                    assert cursor[o] >= o * L, "overloaded rank ran out of copies"
+                    continue
             t = min(left, need)
             f.pieces.append((e, left - t, left))  # the highest remaining ordinals
             migrated[e] += t

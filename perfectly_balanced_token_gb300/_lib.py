@@ -30,7 +30,7 @@ class MoonepError(RuntimeError):
 
 
 class moonep_dims(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("R", "E", "B", "K", "S", "H", "Hp", "mode")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("R", "E", "B", "K", "S", "H", "Hp", "mode", "policy")]
 
     @property
     def L(self):
@@ -104,8 +104,8 @@ def status_string(status: int) -> str:
         return "library not loaded"
 
 
-def dims(R, E, B, K, S, H, Hp, mode=0) -> moonep_dims:
-    return moonep_dims(R, E, B, K, S, H, Hp, mode)
+def dims(R, E, B, K, S, H, Hp, mode=0, policy=0) -> moonep_dims:
+    return moonep_dims(R, E, B, K, S, H, Hp, mode, policy)
 
 
 def _check(rc: int, what: str):

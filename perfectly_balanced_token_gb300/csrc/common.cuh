@@ -10,8 +10,13 @@ namespace moonep {
 
 constexpr int kMaxExperts = 4096;   // smem histograms hold E counters per warp
 constexpr int kChunkCopies = 4096;  // copies per histogram chunk (rounded to tokens)
-constexpr int kTileM = 256;         // rows per GEMM work tile: two M=128 MMA accumulators
 constexpr int kMmaM = 128;          // rows of one tcgen05.mma (cta_group::1)
+// GEMM work-tile height, chosen before launch from the expected rows per
+// weight row group, C*R/E: groups of at least this many rows use 256-row work
+// tiles (two accumulators share each weight panel: fewer L2->SM bytes per
+// flop); smaller groups use 128-row tiles, which keep fewer groups' weights in
+// flight at once and so hit L2 more often.
+constexpr int kBigGroupRows = 4096;
 constexpr int kHistWarps = 8;
 
 // Per-expert migrated range of global ordinals [lo, hi) and where it goes.
@@ -19,7 +24,7 @@ struct Piece {
   int32_t lo, hi, u, g;
 };
 
-// One GEMM work tile of up to kTileM rows: recv/y row of its first row, valid rows, the weight
+// One GEMM work tile of up to Dims::tile_m rows: recv/y row of its first row, valid rows, the weight
 // it multiplies (>= 0: home expert id; < 0: -1 - slot id u*B+j) and its rank.
 struct MTile {
   int32_t row0, rows, wsel, u;
@@ -55,9 +60,10 @@ struct PlanPtrs {
 };
 
 struct Dims {
-  int R, E, B, K, S, H, Hp, mode;
+  int R, E, B, K, S, H, Hp, mode, policy;
   int L, C, N;
   int nchunk, chunk_tokens, max_mtiles;
+  int tile_m;  // GEMM work-tile height: 128 or 256 rows
 };
 
 // Workspace layout (host computes it; kernels receive resolved pointers).

@@ -40,15 +40,19 @@ constexpr int kBK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle ro
 constexpr int kUmmaK = 16;     // K of one tcgen05.mma for 16-bit inputs
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitNs = 4000000000ull;  // 4 s per barrier wait
-// L2 policy: an A (recv) box is dead once the CTAs on its column tiles have read
-// it, so it is loaded evict-first; Y is written with streaming stores; the
-// weight panels, reused by every row tile of their group, keep normal priority.
-constexpr bool kAEvictFirst = true;
-constexpr bool kBEvictLast = false;
-constexpr bool kYStreaming = true;
 
 template <int BN, int STAGES>
-struct GemmCfg {
+struct GemmCfgM128 {  // one 128-row tile, double-buffered accumulator
+  static constexpr int kABytes = kMmaM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
+};
+
+template <int BN, int STAGES>
+struct GemmCfgM256 {  // two 128-row halves sharing each B stage
   static constexpr int kAHalf = kMmaM * kBK * 2;       // one 128-row A box
   static constexpr int kABytes = 2 * kAHalf;
   static constexpr int kBBytes = BN * kBK * 2;
@@ -114,24 +118,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                 int c0, int c1, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -208,11 +194,187 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// One 128-row tile per work item; the accumulator is double buffered so the
+// epilogue of one tile overlaps the main loop of the next.
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
+k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
         const __grid_constant__ CUtensorMap tm_ws, Dims d, PlanPtrs p, uint16_t* __restrict__ y) {
-  using Cfg = GemmCfg<BN, STAGES>;
+  using Cfg = GemmCfgM128<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
+  const int NT = d.Hp / BN;
+  const int total = p.counters[MOONEP_CNT_MTILES] * NT;
+  const int KB = d.H / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_wh);
+    prefetch_tmap(&tm_ws);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const MTile mt = p.mtiles[t / NT];
+        const int n0 = (t % NT) * BN;
+        const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
+        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * d.H;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(full(stage), Cfg::kStageBytes);
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        // wait (time-bounded) for the copies this thread started
+        for (int i = 0; i < min(issued, STAGES); ++i) {
+          if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+          mbar_wait(full(stage), phase, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kMmaM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
+            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            umma_bf16(dtm, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit(empty(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        umma_commit(drain);  // completes once every MMA issued so far is done
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lanes 32q..32q+31 are this warp's rows
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const MTile mt = p.mtiles[t / NT];
+      const int n0 = (t % NT) * BN;
+      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int row = q * 32 + lane;
+      const bool valid = row < mt.rows;
+      uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tbase + c * 32, r);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+            o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+            o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+            o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// Two 128-row halves per work item sharing each B stage.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
+             const __grid_constant__ CUtensorMap tm_ws, Dims d, PlanPtrs p, uint16_t* __restrict__ y) {
+  using Cfg = GemmCfgM256<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
@@ -263,8 +425,6 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint64_t pol_a = l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_last();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN;
@@ -276,22 +436,11 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           mbar_expect_tx(full(stage), bytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
-          if (kAEvictFirst) {
-            tma_load_2d_hint(sa, &tm_a, full(stage), kb * kBK, mt.row0, pol_a);
-            if (two)
-              tma_load_2d_hint(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM, pol_a);
-          } else {
-            tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
-            if (two) tma_load_2d(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM);
-          }
+          tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
+          if (two) tma_load_2d(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM);
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i) {
-            if (kBEvictLast)
-              tma_load_2d_hint(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64,
-                               wrow + kb * kBK, pol_b);
-            else
-              tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
-          }
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -391,8 +540,7 @@ k_ggemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtens
                 o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
                 o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
                 o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
-                if (kYStreaming) __stcs(dst + v, o);
-                else dst[v] = o;
+                dst[v] = o;
               }
             }
           }
@@ -469,20 +617,29 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
-static cudaError_t launch_ggemm_cfg(const Dims& d, const PlanPtrs& p, const CUtensorMap& a,
-                                    const CUtensorMap& wh, const CUtensorMap& ws, uint16_t* y,
-                                    int grid, cudaStream_t st) {
-  using Cfg = GemmCfg<BN, STAGES>;
-  static bool attr_set = false;
+template <typename Cfg, typename KernelT>
+static cudaError_t launch_cfg(KernelT kernel, bool& attr_set, const Dims& d, const PlanPtrs& p,
+                              const CUtensorMap& a, const CUtensorMap& wh, const CUtensorMap& ws,
+                              uint16_t* y, int grid, cudaStream_t st) {
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_ggemm<BN, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_ggemm<BN, STAGES><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, p, y);
+  kernel<<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, p, y);
   return cudaGetLastError();
+}
+
+template <int BN, int S128, int S256>
+static cudaError_t launch_bn(const Dims& d, const PlanPtrs& p, const CUtensorMap& a,
+                             const CUtensorMap& wh, const CUtensorMap& ws, uint16_t* y, int grid,
+                             cudaStream_t st) {
+  static bool set128 = false, set256 = false;
+  if (d.tile_m == 256)
+    return launch_cfg<GemmCfgM256<BN, S256>>(k_ggemm_m256<BN, S256>, set256, d, p, a, wh, ws, y,
+                                             grid, st);
+  return launch_cfg<GemmCfgM128<BN, S128>>(k_ggemm_m128<BN, S128>, set128, d, p, a, wh, ws, y, grid,
+                                           st);
 }
 
 cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* recv,
@@ -501,9 +658,9 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
   const long long max_tiles = (long long)d.max_mtiles * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sms, std::max<long long>(1, max_tiles));
   cudaError_t e;
-  if (bn == 256) e = launch_ggemm_cfg<256, 3>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else if (bn == 128) e = launch_ggemm_cfg<128, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else e = launch_ggemm_cfg<64, 5>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  if (bn == 256) e = launch_bn<256, 4, 3>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else if (bn == 128) e = launch_bn<128, 6, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else e = launch_bn<64, 8, 5>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
   if (e == cudaSuccess) *launches += 1;
   return e;
 }

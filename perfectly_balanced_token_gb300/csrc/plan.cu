@@ -149,19 +149,38 @@ k_plan(Dims d, PlanPtrs p) {
     bool ok = true;
     while (ok) {
       int u = -1, o = -1;
-      for (int h = 0; h < d.R && (u < 0 || o < 0); ++h) {
-        if (u < 0 && sState[h] == kUnder) u = h;
-        if (o < 0 && sState[h] == kOver) o = h;
+      if (d.policy == 1) {  // largest deficit from largest surplus, ties to the smallest id
+        int best_def = 0, best_sur = 0;
+        for (int h = 0; h < d.R; ++h) {
+          if (sState[h] == kUnder && d.C - sLoad[h] > best_def) { best_def = d.C - sLoad[h]; u = h; }
+          if (sState[h] == kOver && sLoad[h] - d.C > best_sur) { best_sur = sLoad[h] - d.C; o = h; }
+        }
+      } else {
+        for (int h = 0; h < d.R && (u < 0 || o < 0); ++h) {
+          if (u < 0 && sState[h] == kUnder) u = h;
+          if (o < 0 && sState[h] == kOver) o = h;
+        }
       }
       if (u < 0) break;
       if (o < 0 || nfill >= d.R - 1) { ok = false; break; }
       const int dcopies = d.C - sLoad[u];
       int need = dcopies, j = 0;
       while (need > 0) {
-        const int e = sCur[o];
-        if (e < o * d.L) { ok = false; break; }
-        const int left = sT[e] - sMig[e];
-        if (left == 0) { sCur[o] = e - 1; continue; }
+        int e, left;
+        if (d.policy == 1) {  // the donor expert with the most copies left, ties to the highest id
+          e = -1;
+          left = 0;
+          for (int c = o * d.L; c < (o + 1) * d.L; ++c) {
+            const int lc = sT[c] - sMig[c];
+            if (lc > 0 && lc >= left) { left = lc; e = c; }
+          }
+          if (e < 0) { ok = false; break; }
+        } else {
+          e = sCur[o];
+          if (e < o * d.L) { ok = false; break; }
+          left = sT[e] - sMig[e];
+          if (left == 0) { sCur[o] = e - 1; continue; }
+        }
         const int t = min(left, need);
         const int g = (j < d.B) ? d.E + j : e;  // slot, or inference overflow row
         if (j < d.B) p.slot_expert[u * d.B + j] = e;
@@ -170,7 +189,7 @@ k_plan(Dims d, PlanPtrs p) {
         p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
         sPieceN[e] = pi + 1;
         p.cu[(size_t)u * (EB + 1) + g + 1] = t;
-        sTiles[u] += (t + kTileM - 1) / kTileM;
+        sTiles[u] += (t + d.tile_m - 1) / d.tile_m;
         sMig[e] += t;
         need -= t;
         ++j;
@@ -201,7 +220,7 @@ k_plan(Dims d, PlanPtrs p) {
     p.keep[e] = k;
     const int h = e / d.L;
     p.cu[(size_t)h * (EB + 1) + e + 1] = k;
-    atomicAdd(&sTiles[h], (k + kTileM - 1) / kTileM);
+    atomicAdd(&sTiles[h], (k + d.tile_m - 1) / d.tile_m);
   }
   // reduce lists: the slots holding e in ascending (u, j)
   for (int s = tid; s < d.R * d.B; s += nt) {
@@ -300,7 +319,7 @@ k_tables(Dims d, PlanPtrs p) {
     const int rows = cu[g + 1];
     if (i < 8) rows_local[i] = rows;
     rsum += rows;
-    tsum += (rows + kTileM - 1) / kTileM;
+    tsum += (rows + d.tile_m - 1) / d.tile_m;
   }
   int ra = rsum, tb = tsum;
   block_scan2<1024>(ra, tb, sa, sb);
@@ -310,8 +329,8 @@ k_tables(Dims d, PlanPtrs p) {
     const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 5 for E <= 4096
     cu[g] = row;
     const int wsel = (g < d.E) ? g : -1 - (u * d.B + (g - d.E));
-    for (int m = 0; m * kTileM < rows; ++m) {
-      p.mtiles[tile++] = MTile{u * d.C + row + m * kTileM, min(kTileM, rows - m * kTileM), wsel, u};
+    for (int m = 0; m * d.tile_m < rows; ++m) {
+      p.mtiles[tile++] = MTile{u * d.C + row + m * d.tile_m, min(d.tile_m, rows - m * d.tile_m), wsel, u};
     }
     row += rows;
   }

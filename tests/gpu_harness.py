@@ -23,12 +23,13 @@ def ensure_library():
     mx.library()
 
 
-def odims(w) -> oplanner.Dims:
-    return oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp, mode=w.mode)
+def odims(w, policy=0) -> oplanner.Dims:
+    return oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp, mode=w.mode,
+                         policy=policy)
 
 
-def cdims(w):
-    return mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode)
+def cdims(w, policy=0):
+    return mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy)
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, what: str):
@@ -73,8 +74,8 @@ def compare_plan(tabs: dict, fp: dict, d: oplanner.Dims):
 class Run:
     """Device buffers and one pass of the CUDA path for a workload."""
 
-    def __init__(self, w, routing, seed=0, guard=4096):
-        self.w, self.d, self.od = w, cdims(w), odims(w)
+    def __init__(self, w, routing, seed=0, guard=4096, policy=0):
+        self.w, self.d, self.od = w, cdims(w, policy), odims(w, policy)
         self.routing = routing
         dev = "cuda"
         self.ws = mx.PlanWorkspace(self.d)

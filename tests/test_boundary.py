@@ -58,7 +58,8 @@ def test_dims_validation():
         with pytest.raises(mx.MoonepError) as ei:
             mx.moonep_plan_workspace_bytes(d)
         assert ei.value.status == _lib.ERR_SHAPE
-    for d in [mx.dims(0, 8, 2, 2, 16, 64, 64), mx.dims(4, 8, -1, 2, 16, 64, 64, 1)]:
+    for d in [mx.dims(0, 8, 2, 2, 16, 64, 64), mx.dims(4, 8, -1, 2, 16, 64, 64, 1),
+              mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 2)]:
         with pytest.raises(mx.MoonepError) as ei:
             mx.moonep_plan_workspace_bytes(d)
         assert ei.value.status == _lib.ERR_ARG

@@ -48,6 +48,13 @@ CASES = [
     ("hot-rank-chain", W("chain", R=8, E=32, B=4, K=2, S=256, H=128, Hp=256),
      lambda w: syn.Routing(((np.arange(w.R * w.S * w.K).reshape(w.R, w.S, w.K)) % 4).astype(np.int32),
                            np.full((w.R, w.S, w.K), 0.5, np.float32))),
+    # C*R/E >= 4096: the GEMM runs 256-row work tiles (two accumulators)
+    ("m256-bn256", W("m256", R=2, E=4, B=2, K=2, S=4096, H=128, Hp=256),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.5, seed=7)),
+    ("m256-bn64-ragged", W("m256b", R=4, E=8, B=2, K=2, S=8192, H=64, Hp=192),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=2.5, seed=8)),
+    ("m256-infer-b0", W("m256i", R=2, E=4, B=0, K=1, S=9000, H=64, Hp=128, mode=1),
+     lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=2)),
 ]
 
 
@@ -202,4 +209,29 @@ def test_send_once_route_and_dispatch(name, w, mk):
     assert np.array_equal(gh.host_bits(run.recv).reshape(w.N, w.H), want)
     got_w = recv_w.cpu().numpy()
     assert np.array_equal(got_w[fp["dst"].reshape(-1)], rt.gates.reshape(-1))
+    run.check_all_guards()
+
+
+@pytest.mark.parametrize("name,w,mk", CASES, ids=[c[0] for c in CASES])
+def test_largest_first_policy_parity(name, w, mk):
+    """Planner policy 1 (largest first): tables bit-exact with the oracle's,
+    Theorem 1 invariants on the GPU's own tables, and the layer outputs still
+    equal the plan-free definitions."""
+    rt = mk(w)
+    od = gh.odims(w, policy=1)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt, policy=1)
+    run.forward()
+    tabs = run.ws.tables()
+    gh.compare_plan(tabs, fp, od)
+    check_plan_arrays(rt.idx, w.R, w.E, w.B, w.K, w.S, w.mode, T=tabs["T"],
+                      n_fills=int(tabs["counters"][0]), fills=tabs["fills"], keep=tabs["keep"],
+                      slot_expert=tabs["slot_expert"], n_recv=tabs["n_recv"], src=tabs["src"],
+                      cu_seqlens=tabs["cu_seqlens"], dst=tabs["dst"], inverse=tabs["inverse"],
+                      gidx=tabs["gidx"])
+    x_bits, w_bits = gh.host_bits(run.x), gh.host_bits(run.w_home)
+    per_e = olayer.expert_outputs(x_bits, w_bits, rt.idx, od)
+    out_want = olayer.combine_from_copies(per_e, rt.gates, od)
+    gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(out_want),
+                    f"{name} combine (policy 1)")
     run.check_all_guards()

@@ -239,3 +239,66 @@ def test_route_encoding_invariants(seed):
     tr = planner.link_traffic(fp["dst"], d, payload_bytes=2 * 64)
     assert tr["send_once_bytes"] <= tr["per_entry_bytes"]
     assert tr["remote_pairs"] <= tr["remote_entries"]
+
+
+# ---- the largest-first policy --------------------------------------------------
+
+def _min_items_covering(sizes, need):
+    """Fewest items whose sizes sum to at least `need` (brute force)."""
+    from itertools import combinations
+    for k in range(len(sizes) + 1):
+        if any(sum(c) >= need for c in combinations(sizes, k)):
+            return k
+    return None
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_largest_first_each_fill_uses_the_fewest_experts(seed):
+    R, E, K, S = 4, 24, 3, 40
+    d = Dims(R=R, E=E, B=E // R, K=K, S=S, policy=1)
+    rt = syn.gumbel_topk_routing(R, S, K, E, alpha=1.5 + 0.2 * seed, seed=seed)
+    _, T, _ = planner.histogram(rt.idx, d)
+    fills, _ = planner.constructive_plan(T, d)
+    # replay: before each fill, the donor's remaining copies per expert
+    remaining = [int(x) for x in T]
+    for f in fills:
+        sizes = [remaining[e] for e in range(f.o * d.L, (f.o + 1) * d.L) if remaining[e] > 0]
+        assert len(f.pieces) == _min_items_covering(sizes, f.d)
+        for e, lo, hi in f.pieces:
+            remaining[e] -= hi - lo
+    _full(rt.idx, d)  # and Theorem 1's invariants still hold
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_largest_first_against_brute_force_and_constructive(seed):
+    R, E, K, S = 3, 6, 2, 8
+    d0 = Dims(R=R, E=E, B=2, K=K, S=S)
+    d1 = Dims(R=R, E=E, B=2, K=K, S=S, policy=1)
+    rt = syn.gumbel_topk_routing(R, S, K, E, alpha=1.0 + seed * 0.5, seed=seed)
+    _, T, _ = planner.histogram(rt.idx, d0)
+    m, _ = theory.min_max_redundant(T, R, d0.C, m_max=d0.L)
+    got1 = int(max(planner.build_plan(rt.idx, d1).n_recv))
+    assert m <= got1 <= d0.L
+
+
+def test_largest_first_is_never_worse_in_total_over_a_sweep():
+    R, E, B, K, S = 8, 64, 8, 4, 512
+    tot0 = tot1 = 0
+    for seed, alpha in enumerate((0.5, 1.0, 1.5, 2.0, 3.0)):
+        rt = syn.gumbel_topk_routing(R, S, K, E, alpha=alpha, seed=seed)
+        p0 = planner.build_plan(rt.idx, Dims(R=R, E=E, B=B, K=K, S=S))
+        p1 = planner.build_plan(rt.idx, Dims(R=R, E=E, B=B, K=K, S=S, policy=1))
+        assert len(p1.fills) <= R - 1 and max(p1.n_recv) <= E // R
+        tot0 += int(p0.n_recv.sum())
+        tot1 += int(p1.n_recv.sum())
+    assert tot1 <= tot0
+
+
+def test_largest_first_on_the_theorem2_case_reaches_the_bound():
+    R, E, K, S = 8, 384, 8, 8192
+    d = Dims(R=R, E=E, B=E // R, K=K, S=S, policy=1)
+    rt = syn.round_robin_routing(R, S, K, E, first=E // R)
+    p = planner.build_plan(rt.idx, d)
+    # rank 0 owns nothing, so any plan gives it >= ceil(E(R-1)/R^2) = 42 experts
+    assert p.n_recv[0] >= theory.theorem2_bound(R, E)
+    assert max(p.n_recv) <= E // R
