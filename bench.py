@@ -68,6 +68,23 @@ WORKLOADS = {"pages": _pages, "k3": _k3, "profile": _profile_workload,
 DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,), "profile128": (1.0,)}
 
 
+def measured_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from an ncu capture recorded under
+    profiles/, or None if there is none or the GEMM source changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    src = os.path.join(ROOT, "perfectly_balanced_token_gb300", "csrc", "gemm.cu")
+    if not (os.path.exists(p) and os.path.exists(src)):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if not rec or rec.get("gemm_cu_sha256") != sha:
+        return None
+    return rec
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -335,11 +352,14 @@ def run_ours(args):
     gemm_ms = float(seg[:, 3].mean())
     flops = 2.0 * N * w.H * w.Hp
     achieved_tf = flops / (gemm_ms / 1e3) / 1e12
-    roofline = {"kernel": "k_ggemm (moonep_grouped_gemm)", "bound": "tensor",
+    gemm_kernel = "k_ggemm_m256" if (w.S * w.K * w.R >= 4096 * w.E) else "k_ggemm_m128"
+    traffic = measured_traffic(gemm_kernel) if args.workload == "pages" else None
+    roofline = {"kernel": f"{gemm_kernel} (moonep_grouped_gemm)", "bound": "tensor",
                 "achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / bf16_peak, "peak_source": f"bf16_tflops ({peak_src}, burst)",
-                "traffic": None, "algorithmic_flops_per_launch": flops,
-                "ms_per_launch": gemm_ms}
+                "traffic": traffic["bytes_per_launch"] if traffic else None,
+                "traffic_source": traffic["source"] if traffic else None,
+                "algorithmic_flops_per_launch": flops, "ms_per_launch": gemm_ms}
     occ = np.mean([c["occupied_slots"] for c in counters])
     red = np.mean([c["reduced_experts"] for c in counters])
     hh = w.H * w.Hp

@@ -12,6 +12,10 @@
  *   moonep_combine           fused unpermute, weighted by the top-K gates
  *   moonep_reduce_grad       fold the slot gradients back into the home rows
  *
+ * and its backward: moonep_combine_backward, moonep_grouped_gemm_dx,
+ * moonep_grouped_gemm_dw (which writes the slot gradients reduce_grad folds)
+ * and moonep_dispatch_backward.
+ *
  * Symbols: R ranks, E experts, L = E/R experts homed on each rank
  * (home(e) = e / L), B prefetch slots per rank, K experts per token, S tokens
  * per rank, C = S*K copies per rank, N = R*C copies in all, H the hidden size,
@@ -98,6 +102,8 @@ typedef struct moonep_plan_layout {
   size_t route;        /* int32[R][S][K] send-once route entries: the copy's row
                           offset on its destination rank, or -offset-1 when an
                           earlier entry of the same token already goes there  */
+  size_t groups;       /* internal: non-empty (rank, weight row) groups, int32[4]
+                          each (first row, rows, weight row, rank)             */
 } moonep_plan_layout;
 
 /* Index of each counter in the `counters` table. */
@@ -107,7 +113,8 @@ enum moonep_counter {
   MOONEP_CNT_OCCUPIED = 2, /* occupied prefetch slots                      */
   MOONEP_CNT_REDUCE = 3,   /* home experts with at least one slot copy     */
   MOONEP_CNT_REMOTE_ENTRIES = 4, /* route entries whose destination is not the token's own rank */
-  MOONEP_CNT_REMOTE_PAIRS = 5    /* distinct (token, destination rank) pairs among those       */
+  MOONEP_CNT_REMOTE_PAIRS = 5,   /* distinct (token, destination rank) pairs among those       */
+  MOONEP_CNT_GROUPS = 6          /* non-empty (rank, weight row) groups                         */
 };
 
 /* Size in bytes of the plan workspace for `dims` (host only, no CUDA call).
@@ -204,6 +211,48 @@ int moonep_combine(const moonep_dims* dims, void* plan_ws, const uint16_t* y,
  * g_home : fp32 [E][H][Hp] (updated).  g_slot : fp32 [R][B][H][Hp] (updated). */
 int moonep_reduce_grad(const moonep_dims* dims, void* plan_ws, float* g_home,
                        float* g_slot, void* stream);
+
+/* ---- backward of the layer ------------------------------------------------
+ * The routed-expert backward that produces the slot gradients reduce_grad
+ * folds ("Moonshot AI 开源 MoonEP", contract paragraph: training keeps fp32
+ * [E+B, H, H'] gradients whose rows [E, E+B) are separate reduce buffers;
+ * "MoonEP : l'équilibrage parfait", section L'idée: in the backward pass the
+ * redundant experts' gradients are staged in a local reduce buffer and
+ * reduced to their home ranks afterwards).  All four use the plan of the
+ * forward pass. */
+
+/* Backward of moonep_combine: dY[dst[r][s][k]] = bf16(gates[r][s][k] *
+ * d_out[r][s]) and d_gates[r][s][k] = sum over h of y[dst[r][s][k]][h] *
+ * d_out[r][s][h] (fp32).  y, d_y : bf16 [R][C][Hp].  gates, d_gates : fp32
+ * [R][S][K].  d_out : bf16 [R][S][Hp].  Requires K <= 128 and Hp <= 8192
+ * (MOONEP_ERR_SHAPE otherwise). */
+int moonep_combine_backward(const moonep_dims* dims, void* plan_ws, const uint16_t* y,
+                            const float* gates, const uint16_t* d_out, uint16_t* d_y,
+                            float* d_gates, void* stream);
+
+/* Input gradient of the grouped GEMM: for each rank u and group g,
+ * d_recv[rows of g] = d_y[rows of g] . W(u,g)^T (fp32 accumulation, bf16 out);
+ * W(u,g) as in moonep_grouped_gemm.  d_y : bf16 [R][C][Hp].  d_recv : bf16
+ * [R][C][H]. */
+int moonep_grouped_gemm_dx(const moonep_dims* dims, void* plan_ws, const uint16_t* d_y,
+                           const uint16_t* w_home, const uint16_t* w_slot, uint16_t* d_recv,
+                           void* stream);
+
+/* Weight gradient of the grouped GEMM: for each non-empty group (u, g),
+ * G(u,g) += recv[rows of g]^T . d_y[rows of g] in fp32, where G(u,g) is
+ * g_home[g] for a home group and g_slot[u][g-E] for a slot group; reduce_grad
+ * then folds the slots into their home rows.  recv : bf16 [R][C][H].
+ * g_home : fp32 [E][H][Hp], g_slot : fp32 [R][B][H][Hp] (both updated).
+ * Training mode only (MOONEP_ERR_ARG in mode 1); H must be a multiple of 128
+ * (MOONEP_ERR_SHAPE). */
+int moonep_grouped_gemm_dw(const moonep_dims* dims, void* plan_ws, const uint16_t* recv,
+                           const uint16_t* d_y, float* g_home, float* g_slot, void* stream);
+
+/* Backward of moonep_dispatch: d_x[r][s] = bf16( sum over k ascending of
+ * d_recv[dst[r][s][k]] ) (fp32 sums).  d_recv : bf16 [R][C][H].  d_x : bf16
+ * [R][S][H]. */
+int moonep_dispatch_backward(const moonep_dims* dims, void* plan_ws, const uint16_t* d_recv,
+                             uint16_t* d_x, void* stream);
 
 /* Copy the workspace status word to *host_status.  SYNCHRONISES the stream. */
 int moonep_read_status(const moonep_dims* dims, const void* plan_ws,

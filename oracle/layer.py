@@ -176,3 +176,83 @@ def reduce_grad(g_home: np.ndarray, g_slot: np.ndarray, plan: Plan,
                     acc = acc + g_slot[u, j].astype(np.float32)
                     g_slot[u, j] = 0.0
         g_home[e] = acc
+
+
+# -- backward ---------------------------------------------------------------------
+# The routed-expert backward that produces the slot gradients reduce_grad folds
+# ("Moonshot AI 开源 MoonEP", contract paragraph: training keeps fp32 [E+B, H, H']
+# gradients whose rows [E, E+B) are the reduce buffers; MoonEP : l'équilibrage
+# parfait, "L'idée": in the backward pass the redundant experts' gradients are
+# staged in a local reduce buffer and reduced to their home ranks afterwards).
+# Written per copy, independent of any plan; with fp64 accumulation and one
+# rounding to bf16 for bf16 outputs (readings: the pages fix no precision).
+
+def combine_backward(y_copy_bits: np.ndarray, dout_bits: np.ndarray, gates: np.ndarray,
+                     d: Dims):
+    """For out[t] = sum_k g[t,k] * Y[t,k]:  dY[t,k] = bf16(g[t,k] * dout[t]) and
+    dg[t,k] = <Y[t,k], dout[t]>.  y_copy_bits is [N, H'] in copy order."""
+    g = gates.reshape(d.N).astype(np.float64)
+    dout = bf16_to_f64(dout_bits.reshape(d.R * d.S, d.Hp))
+    tok = np.arange(d.N) // d.K
+    dy = to_bf16(g[:, None] * dout[tok])
+    dg = np.einsum("ch,ch->c", bf16_to_f64(y_copy_bits.reshape(d.N, d.Hp)), dout[tok])
+    return dy, dg.reshape(d.R, d.S, d.K)
+
+
+def expert_backward(x_bits: np.ndarray, w_bits, idx: np.ndarray, dy_copy_bits: np.ndarray,
+                    d: Dims, experts=None) -> dict:
+    """Per expert e: dRecv rows = bf16(dY @ W_e^T) for its copies, and
+    dW_e = sum over its copies of x_token^T dY (fp64, [H, H'])."""
+    flat = idx.reshape(-1)
+    xs = bf16_to_f64(x_bits.reshape(d.R * d.S, d.H))
+    dyc = bf16_to_f64(dy_copy_bits.reshape(d.N, d.Hp))
+    out = {}
+    for e in (range(d.E) if experts is None else experts):
+        cids = np.nonzero(flat == e)[0]
+        w = bf16_to_f64(w_bits(e) if callable(w_bits) else w_bits[e])
+        drecv = to_bf16(dyc[cids] @ w.T)
+        dw = xs[cids // d.K].T @ dyc[cids]
+        out[e] = (cids, drecv, dw)
+    return out
+
+
+def dispatch_backward(drecv_copy_bits: np.ndarray, d: Dims) -> np.ndarray:
+    """dx[t] = bf16( sum over k ascending of dRecv[t,k] ), [N, H] in copy order in."""
+    r = bf16_to_f64(drecv_copy_bits.reshape(d.R * d.S, d.K, d.H))
+    return to_bf16(r.sum(axis=1))
+
+
+def dw_by_group(x_bits: np.ndarray, idx: np.ndarray, dy_copy_bits: np.ndarray, plan: Plan,
+                dst: np.ndarray) -> dict:
+    """The same weight gradient split the way the grouped GEMM produces it before
+    reduce_grad: each (rank u, weight row g) group sums its own rows only.
+    Returns {(u, g): [H, H'] fp64} for non-empty groups."""
+    d = plan.dims
+    xs = bf16_to_f64(x_bits.reshape(d.R * d.S, d.H))
+    dyc = bf16_to_f64(dy_copy_bits.reshape(d.N, d.Hp))
+    dflat = dst.reshape(-1)
+    out = {}
+    for u in range(d.R):
+        for g in range(d.E + d.B):
+            a0, a1 = plan.cu_seqlens[u, g], plan.cu_seqlens[u, g + 1]
+            if a1 == a0:
+                continue
+            rows = set(range(u * d.C + a0, u * d.C + a1))
+            cids = np.array([c for c in range(d.N) if dflat[c] in rows])
+            out[(u, g)] = xs[cids // d.K].T @ dyc[cids]
+    return out
+
+
+def grouped_gemm_dw_rows(recv_bits: np.ndarray, dy_rows_bits: np.ndarray, plan: Plan) -> dict:
+    """{(u, g): recv[rows of g]^T . dY[rows of g]} (fp64) over every rank's
+    buffer, from its cu_seqlens, for non-empty groups."""
+    d = plan.dims
+    out = {}
+    for u in range(d.R):
+        for g in range(d.E + d.B):
+            a0, a1 = plan.cu_seqlens[u, g], plan.cu_seqlens[u, g + 1]
+            if a1 == a0:
+                continue
+            rows = slice(u * d.C + a0, u * d.C + a1)
+            out[(u, g)] = bf16_to_f64(recv_bits[rows]).T @ bf16_to_f64(dy_rows_bits[rows])
+    return out

@@ -20,7 +20,7 @@ OK = 0
 ERR_ARG, ERR_ALIGN, ERR_SLOTS, ERR_SHAPE, ERR_CUDA, ERR_SCRATCH = 1, 2, 3, 4, 5, 6
 ERR_ROUTING, ERR_INTERNAL, ERR_TIMEOUT = 0x100, 0x200, 0x400
 CNT_FILLS, CNT_MTILES, CNT_OCCUPIED, CNT_REDUCE = 0, 1, 2, 3
-CNT_REMOTE_ENTRIES, CNT_REMOTE_PAIRS = 4, 5
+CNT_REMOTE_ENTRIES, CNT_REMOTE_PAIRS, CNT_GROUPS = 4, 5, 6
 
 
 class MoonepError(RuntimeError):
@@ -48,12 +48,13 @@ class moonep_dims(ctypes.Structure):
 _SIZE_FIELDS = ("total_bytes", "status", "counters", "counts", "T", "load", "keep", "gidx",
                 "fills", "slot_expert", "n_recv", "src", "cu_seqlens", "dst", "inverse",
                 "pieces", "occupied", "reduce", "mtiles")
-_LAYOUT_FIELDS = _SIZE_FIELDS + ("route",)  # total size, then every table offset
+_LAYOUT_FIELDS = _SIZE_FIELDS + ("route", "groups")  # total size, then every table offset
 
 
 class moonep_plan_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in _SIZE_FIELDS] + [
-        ("nchunk", ctypes.c_int32), ("max_mtiles", ctypes.c_int32), ("route", ctypes.c_size_t)]
+        ("nchunk", ctypes.c_int32), ("max_mtiles", ctypes.c_int32), ("route", ctypes.c_size_t),
+        ("groups", ctypes.c_size_t)]
 
 
 _lib = None
@@ -82,6 +83,10 @@ def library() -> ctypes.CDLL:
         "moonep_read_status": [D, P, ctypes.POINTER(ctypes.c_int32), P],
         "moonep_plan_export": [D, P, P, P],
         "moonep_plan_noalloc": [D, P, P, P],
+        "moonep_combine_backward": [D, P, P, P, P, P, P, P],
+        "moonep_grouped_gemm_dx": [D, P, P, P, P, P, P],
+        "moonep_grouped_gemm_dw": [D, P, P, P, P, P, P],
+        "moonep_dispatch_backward": [D, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -212,6 +217,41 @@ def moonep_reduce_grad(d, plan_ws, g_home, g_slot, stream=None):
         ctypes.byref(d), _ws(d, plan_ws), _ptr(g_home, torch.float32, d.E * hh, "g_home"),
         _ptr(g_slot, torch.float32, d.R * d.B * hh, "g_slot", allow_none=d.B == 0),
         _stream(stream)), "moonep_reduce_grad")
+
+
+def moonep_combine_backward(d, plan_ws, y, gates, d_out, d_y, d_gates, stream=None):
+    _check(library().moonep_combine_backward(
+        ctypes.byref(d), _ws(d, plan_ws), _ptr(y, torch.bfloat16, d.N * d.Hp, "y"),
+        _ptr(gates, torch.float32, d.N, "gates"),
+        _ptr(d_out, torch.bfloat16, d.R * d.S * d.Hp, "d_out"),
+        _ptr(d_y, torch.bfloat16, d.N * d.Hp, "d_y"), _ptr(d_gates, torch.float32, d.N, "d_gates"),
+        _stream(stream)), "moonep_combine_backward")
+
+
+def moonep_grouped_gemm_dx(d, plan_ws, d_y, w_home, w_slot, d_recv, stream=None):
+    hh = d.H * d.Hp
+    _check(library().moonep_grouped_gemm_dx(
+        ctypes.byref(d), _ws(d, plan_ws), _ptr(d_y, torch.bfloat16, d.N * d.Hp, "d_y"),
+        _ptr(w_home, torch.bfloat16, d.E * hh, "w_home"),
+        _ptr(w_slot, torch.bfloat16, d.R * d.B * hh, "w_slot", allow_none=d.B == 0),
+        _ptr(d_recv, torch.bfloat16, d.N * d.H, "d_recv"), _stream(stream)), "moonep_grouped_gemm_dx")
+
+
+def moonep_grouped_gemm_dw(d, plan_ws, recv, d_y, g_home, g_slot, stream=None):
+    hh = d.H * d.Hp
+    _check(library().moonep_grouped_gemm_dw(
+        ctypes.byref(d), _ws(d, plan_ws), _ptr(recv, torch.bfloat16, d.N * d.H, "recv"),
+        _ptr(d_y, torch.bfloat16, d.N * d.Hp, "d_y"),
+        _ptr(g_home, torch.float32, d.E * hh, "g_home"),
+        _ptr(g_slot, torch.float32, d.R * d.B * hh, "g_slot", allow_none=d.B == 0),
+        _stream(stream)), "moonep_grouped_gemm_dw")
+
+
+def moonep_dispatch_backward(d, plan_ws, d_recv, d_x, stream=None):
+    _check(library().moonep_dispatch_backward(
+        ctypes.byref(d), _ws(d, plan_ws), _ptr(d_recv, torch.bfloat16, d.N * d.H, "d_recv"),
+        _ptr(d_x, torch.bfloat16, d.R * d.S * d.H, "d_x"), _stream(stream)),
+        "moonep_dispatch_backward")
 
 
 def moonep_read_status(d, plan_ws, stream=None) -> int:

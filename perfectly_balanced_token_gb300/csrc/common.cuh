@@ -57,19 +57,22 @@ struct PlanPtrs {
   int32_t* red_list;    // [E] experts with >= 1 slot copy
   int32_t* rank_tiles;  // [R+1] tile offset of each rank
   MTile* mtiles;        // [max_mtiles]
+  int32_t* rank_groups; // [R+1] group offset of each rank
+  MTile* groups;        // [max_groups] non-empty (rank, weight row) groups: all rows of each
 };
 
 struct Dims {
   int R, E, B, K, S, H, Hp, mode, policy;
   int L, C, N;
-  int nchunk, chunk_tokens, max_mtiles;
+  int nchunk, chunk_tokens, max_mtiles, max_groups;
   int tile_m;  // GEMM work-tile height: 128 or 256 rows
 };
 
 // Workspace layout (host computes it; kernels receive resolved pointers).
 struct Layout {
   moonep_plan_layout pub;
-  size_t pieces, piece_n, piece_base, home_base, red_slots, red_n, red_list, rank_tiles;
+  size_t pieces, piece_n, piece_base, home_base, red_slots, red_n, red_list, rank_tiles,
+      rank_groups;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -189,17 +189,46 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major (bit 16 =
 // 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn = false, bool b_mn = true) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// Sizes of one grouped product: C[rows x N] = A[rows x K] . B[K x N], with B
+// drawn from a weight tensor of wrows rows per expert.  Forward: K = H,
+// N = H' (B = W, N-major).  Input gradient: K = H', N = H (B = W^T, which is
+// W read K-major).
+struct GemmShape {
+  int K, N, wrows;
+};
+
+// B stage loads and descriptors for the two layouts of the weight operand.
+template <int BN, bool BKM>
+struct BOperand {
+  // N-major: BN/64 boxes of 64(n) x 64(k), 8 KiB apart; K-major: one box of
+  // 64(k) x BN(n) rows of 128 B.
+  static __device__ __forceinline__ void load(uint32_t sb, const CUtensorMap* m, uint32_t bar,
+                                              int n0, int k0, int wrow) {
+    if (BKM) {
+      tma_load_2d(sb, m, bar, k0, wrow + n0);
+    } else {
+#pragma unroll
+      for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, m, bar, n0 + i * 64, wrow + k0);
+    }
+  }
+  static __device__ __forceinline__ uint64_t desc(uint32_t sb, int k) {
+    return BKM ? sw128_desc(sb + k * (kUmmaK * 2), 16, 1024)
+               : sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+  }
+};
 
 // One 128-row tile per work item; the accumulator is double buffered so the
 // epilogue of one tile overlaps the main loop of the next.
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool BKM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
-        const __grid_constant__ CUtensorMap tm_ws, Dims d, PlanPtrs p, uint16_t* __restrict__ y) {
+        const __grid_constant__ CUtensorMap tm_ws, Dims d, GemmShape sh, PlanPtrs p,
+             uint16_t* __restrict__ y) {
   using Cfg = GemmCfgM128<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -215,9 +244,9 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
-  const int NT = d.Hp / BN;
+  const int NT = sh.N / BN;
   const int total = p.counters[MOONEP_CNT_MTILES] * NT;
-  const int KB = d.H / kBK;
+  const int KB = sh.K / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -256,15 +285,13 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN;
         const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
-        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * d.H;
+        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * sh.wrows;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           mbar_expect_tx(full(stage), Cfg::kStageBytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
           tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
-#pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          BOperand<BN, BKM>::load(sa + Cfg::kABytes, wmap, full(stage), n0, kb * kBK, wrow);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -282,7 +309,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kMmaM, BN);
+      constexpr uint32_t idesc = make_idesc(kMmaM, BN, false, !BKM);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -298,7 +325,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
-            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            const uint64_t bd = BOperand<BN, BKM>::desc(sb, k);
             umma_bf16(dtm, ad, bd, idesc, (kb | k) != 0);
           }
           umma_commit(empty(stage));
@@ -334,7 +361,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
       tc_fence_after();
       const int row = q * 32 + lane;
       const bool valid = row < mt.rows;
-      uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
+      uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -370,10 +397,11 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 }
 
 // Two 128-row halves per work item sharing each B stage.
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool BKM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
-             const __grid_constant__ CUtensorMap tm_ws, Dims d, PlanPtrs p, uint16_t* __restrict__ y) {
+             const __grid_constant__ CUtensorMap tm_ws, Dims d, GemmShape sh, PlanPtrs p,
+             uint16_t* __restrict__ y) {
   using Cfg = GemmCfgM256<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -389,9 +417,9 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
-  const int NT = d.Hp / BN;
+  const int NT = sh.N / BN;
   const int total = p.counters[MOONEP_CNT_MTILES] * NT;
-  const int KB = d.H / kBK;
+  const int KB = sh.K / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -430,7 +458,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         const int n0 = (t % NT) * BN;
         const bool two = mt.rows > kMmaM;
         const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
-        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * d.H;
+        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * sh.wrows;
         const uint32_t bytes = Cfg::kAHalf * (two ? 2 : 1) + Cfg::kBBytes;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -438,9 +466,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
           tma_load_2d(sa, &tm_a, full(stage), kb * kBK, mt.row0);
           if (two) tma_load_2d(sa + Cfg::kAHalf, &tm_a, full(stage), kb * kBK, mt.row0 + kMmaM);
-#pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sa + Cfg::kABytes + i * 8192, wmap, full(stage), n0 + i * 64, wrow + kb * kBK);
+          BOperand<BN, BKM>::load(sa + Cfg::kABytes, wmap, full(stage), n0, kb * kBK, wrow);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -458,7 +484,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kMmaM, BN);
+      constexpr uint32_t idesc = make_idesc(kMmaM, BN, false, !BKM);
       int stage = 0;
       uint32_t phase = 0, item = 0;
       bool ok = true;
@@ -475,7 +501,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
-            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            const uint64_t bd = BOperand<BN, BKM>::desc(sb, k);
             umma_bf16(tmem_base, ad, bd, idesc, (kb | k) != 0);
           }
           if (two) {
@@ -486,7 +512,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
               const uint64_t ad = sw128_desc(sa + Cfg::kAHalf + k * (kUmmaK * 2), 16, 1024);
-              const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+              const uint64_t bd = BOperand<BN, BKM>::desc(sb, k);
               umma_bf16(tmem_base + BN, ad, bd, idesc, (kb | k) != 0);
             }
           }
@@ -524,7 +550,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         if (h == 0 || mt.rows > kMmaM) {
           const int row = h * kMmaM + q * 32 + lane;
           const bool valid = row < mt.rows;
-          uint16_t* yrow = y + (size_t)(mt.row0 + row) * d.Hp + n0;
+          uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
           const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * BN);
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
@@ -549,6 +575,234 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty(h));  // every item releases both halves
       }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// Weight gradient of the grouped GEMM: for every non-empty (rank u, weight
+// row g) group with rows a0..a1 of the receive buffer,
+//   G(u,g) += X[a0:a1]^T . dY[a0:a1]        ([H x H'], fp32),
+// where G(u,g) is g_home[g] for a home group and slot (u, g-E) of g_slot for a
+// slot group ("Moonshot AI 开源 MoonEP", contract paragraph: the redundant
+// experts' gradients go to the [R, B, H, H'] reduce buffers that reduce_grad
+// folds into the home rows).  Work items are (group, 128-row tile of H, BN
+// column tile of H'), column tiles fastest, so the CTAs running together read
+// the same group's rows from L2.  Both operands are read N-major straight from
+// the row-major buffers: A = X^T (two 64(h) x 64(row) boxes), B = dY (BN/64
+// boxes of 64(n) x 64(row)).  The reduction runs over the group's rows in
+// 64-row blocks; in the last block the rows past the group's end are zeroed
+// in shared memory before the MMAs.  Accumulators are double buffered in TMEM;
+// the epilogue adds them into G with fp32 read-modify-writes.
+template <int BN, int STAGES>
+struct GemmCfgDW {
+  static constexpr int kABytes = kMmaM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+           Dims d, PlanPtrs p, float* __restrict__ g_home, float* __restrict__ g_slot) {
+  using Cfg = GemmCfgDW<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
+  const int MT = d.H / kMmaM, NT = d.Hp / BN;
+  const int per_group = MT * NT;
+  const int total = p.counters[MOONEP_CNT_GROUPS] * per_group;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_dy);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const MTile grp = p.groups[t / per_group];
+        const int m0 = ((t % per_group) / NT) * kMmaM;
+        const int n0 = (t % NT) * BN;
+        const int KB = (grp.rows + kBK - 1) / kBK;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(full(stage), Cfg::kStageBytes);
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const int r0 = grp.row0 + kb * kBK;
+          tma_load_2d(sa, &tm_x, full(stage), m0, r0);
+          tma_load_2d(sa + 8192, &tm_x, full(stage), m0 + 64, r0);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sa + Cfg::kABytes + i * 8192, &tm_dy, full(stage), n0 + i * 64, r0);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        for (int i = 0; i < min(issued, STAGES); ++i) {
+          if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+          mbar_wait(full(stage), phase, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (lane 0) with partial-block zeroing (all lanes) ----
+    constexpr uint32_t idesc = make_idesc(kMmaM, BN, true, true);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const MTile grp = p.groups[t / per_group];
+      const int KB = (grp.rows + kBK - 1) / kBK;
+      ok = __all_sync(0xffffffffu, mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < KB; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(full(stage), phase, abort_flag));
+        if (!ok) break;
+        uint8_t* st_base = smem + stage * Cfg::kStageBytes;
+        const int valid = grp.rows - kb * kBK;
+        if (valid < kBK) {  // rows past the group's end belong to another group
+          constexpr int kBoxes = 2 + BN / 64;
+          const int per_box = (kBK - valid) * 8;  // uint4 per box
+          for (int i = lane; i < kBoxes * per_box; i += 32) {
+            const int box = i / per_box, j = i % per_box;
+            uint4* z = reinterpret_cast<uint4*>(st_base + box * 8192 + valid * 128) + j;
+            *z = make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sa = smem_u32(st_base);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 128), 8192, 1024);
+            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            umma_bf16(dtm, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit(empty(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(tfull(acc));
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_error(p.status, MOONEP_ERR_TIMEOUT);
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5): G += accumulator ----------------
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const size_t hh = (size_t)d.H * d.Hp;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const MTile grp = p.groups[t / per_group];
+      const int m0 = ((t % per_group) / NT) * kMmaM;
+      const int n0 = (t % NT) * BN;
+      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      float* gbase = grp.wsel >= 0 ? g_home + (size_t)grp.wsel * hh
+                                   : g_slot + (size_t)(-1 - grp.wsel) * hh;
+      float* grow = gbase + (size_t)(m0 + q * 32 + lane) * d.Hp + n0;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; c += 2) {
+        float4 g0[8], g1[8];
+        float4* p0 = reinterpret_cast<float4*>(grow + c * 32);
+        float4* p1 = reinterpret_cast<float4*>(grow + (c + 1) * 32);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          g0[v] = p0[v];
+          g1[v] = p1[v];
+        }
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(tbase + c * 32, r0);
+        tmem_ld_x32(tbase + (c + 1) * 32, r1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          g0[v].x += __uint_as_float(r0[4 * v + 0]);
+          g0[v].y += __uint_as_float(r0[4 * v + 1]);
+          g0[v].z += __uint_as_float(r0[4 * v + 2]);
+          g0[v].w += __uint_as_float(r0[4 * v + 3]);
+          g1[v].x += __uint_as_float(r1[4 * v + 0]);
+          g1[v].y += __uint_as_float(r1[4 * v + 1]);
+          g1[v].z += __uint_as_float(r1[4 * v + 2]);
+          g1[v].w += __uint_as_float(r1[4 * v + 3]);
+          p0[v] = g0[v];
+          p1[v] = g1[v];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -617,50 +871,107 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Cfg, typename KernelT>
-static cudaError_t launch_cfg(KernelT kernel, bool& attr_set, const Dims& d, const PlanPtrs& p,
-                              const CUtensorMap& a, const CUtensorMap& wh, const CUtensorMap& ws,
-                              uint16_t* y, int grid, cudaStream_t st) {
+template <typename Cfg, typename KernelT, typename... Args>
+static cudaError_t launch_cfg(KernelT kernel, bool& attr_set, int grid, cudaStream_t st,
+                              Args... args) {
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kernel<<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, p, y);
+  kernel<<<grid, kGemmThreads, Cfg::kSmem, st>>>(args...);
   return cudaGetLastError();
 }
 
-template <int BN, int S128, int S256>
-static cudaError_t launch_bn(const Dims& d, const PlanPtrs& p, const CUtensorMap& a,
+template <int BN, int S128, int S256, bool BKM>
+static cudaError_t launch_bn(const Dims& d, GemmShape sh, const PlanPtrs& p, const CUtensorMap& a,
                              const CUtensorMap& wh, const CUtensorMap& ws, uint16_t* y, int grid,
                              cudaStream_t st) {
   static bool set128 = false, set256 = false;
   if (d.tile_m == 256)
-    return launch_cfg<GemmCfgM256<BN, S256>>(k_ggemm_m256<BN, S256>, set256, d, p, a, wh, ws, y,
-                                             grid, st);
-  return launch_cfg<GemmCfgM128<BN, S128>>(k_ggemm_m128<BN, S128>, set128, d, p, a, wh, ws, y, grid,
-                                           st);
+    return launch_cfg<GemmCfgM256<BN, S256>>(k_ggemm_m256<BN, S256, BKM>, set256, grid, st, a, wh,
+                                             ws, d, sh, p, y);
+  return launch_cfg<GemmCfgM128<BN, S128>>(k_ggemm_m128<BN, S128, BKM>, set128, grid, st, a, wh, ws,
+                                           d, sh, p, y);
 }
 
+static int sm_count_gemm() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+static int pick_bn(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
+
+// The two weight tensors as 2D [rows][H'] maps with a box of box_outer rows.
+static bool encode_weights(const Dims& d, const void* w_home, const void* w_slot,
+                           uint32_t box_outer, CUtensorMap* twh, CUtensorMap* tws) {
+  if (!encode_2d(twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, box_outer)) return false;
+  const bool slots = (w_slot != nullptr && d.B > 0);
+  return encode_2d(tws, slots ? w_slot : w_home, (uint64_t)d.Hp,
+                   slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, box_outer);
+}
+
+// Forward: Y = recv . W (K = H, N = H', W read N-major).
 cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* recv,
                                 const void* w_home, const void* w_slot, void* y, cudaStream_t st,
                                 int* launches) {
   CUtensorMap ta, twh, tws;
   if (!encode_2d(&ta, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, kMmaM)) return cudaErrorInvalidValue;
-  if (!encode_2d(&twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64)) return cudaErrorInvalidValue;
-  const void* ws = (w_slot != nullptr && d.B > 0) ? w_slot : w_home;
-  const uint64_t ws_rows = (w_slot != nullptr && d.B > 0) ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H;
-  if (!encode_2d(&tws, ws, (uint64_t)d.Hp, ws_rows, 64)) return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int bn = (d.Hp % 256 == 0) ? 256 : (d.Hp % 128 == 0 ? 128 : 64);
+  if (!encode_weights(d, w_home, w_slot, 64, &twh, &tws)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(d.Hp);
   const long long max_tiles = (long long)d.max_mtiles * (d.Hp / bn);
-  const int grid = (int)std::min<long long>(sms, std::max<long long>(1, max_tiles));
+  const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_tiles));
+  const GemmShape sh{d.H, d.Hp, d.H};
   cudaError_t e;
-  if (bn == 256) e = launch_bn<256, 4, 3>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else if (bn == 128) e = launch_bn<128, 6, 4>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else e = launch_bn<64, 8, 5>(d, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  if (bn == 256) e = launch_bn<256, 4, 3, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else if (bn == 128) e = launch_bn<128, 6, 4, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  else e = launch_bn<64, 8, 5, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
+  if (e == cudaSuccess) *launches += 1;
+  return e;
+}
+
+// Input gradient: dRecv = dY . W^T (K = H', N = H, W read K-major).
+cudaError_t launch_grouped_gemm_dx(const Dims& d, const PlanPtrs& p, const void* dy,
+                                   const void* w_home, const void* w_slot, void* d_recv,
+                                   cudaStream_t st, int* launches) {
+  const int bn = pick_bn(d.H);
+  CUtensorMap ta, twh, tws;
+  if (!encode_2d(&ta, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, kMmaM)) return cudaErrorInvalidValue;
+  if (!encode_weights(d, w_home, w_slot, (uint32_t)bn, &twh, &tws)) return cudaErrorInvalidValue;
+  const long long max_tiles = (long long)d.max_mtiles * (d.H / bn);
+  const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_tiles));
+  const GemmShape sh{d.Hp, d.H, d.H};
+  cudaError_t e;
+  if (bn == 256) e = launch_bn<256, 4, 3, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
+  else if (bn == 128) e = launch_bn<128, 6, 4, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
+  else e = launch_bn<64, 8, 5, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
+  if (e == cudaSuccess) *launches += 1;
+  return e;
+}
+
+// Weight gradient: G(u,g) += recv[group rows]^T . dY[group rows].
+cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void* recv,
+                                   const void* dy, float* g_home, float* g_slot, cudaStream_t st,
+                                   int* launches) {
+  CUtensorMap tx, tdy;
+  if (!encode_2d(&tx, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
+  if (!encode_2d(&tdy, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(d.Hp);
+  const long long max_items = (long long)d.max_groups * (d.H / kMmaM) * (d.Hp / bn);
+  const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_items));
+  cudaError_t e;
+  if (bn == 256) {
+    static bool set = false;
+    e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+  } else if (bn == 128) {
+    static bool set = false;
+    e = launch_cfg<GemmCfgDW<128, 6>>(k_ggemm_dw<128, 6>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+  } else {
+    static bool set = false;
+    e = launch_cfg<GemmCfgDW<64, 8>>(k_ggemm_dw<64, 8>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+  }
   if (e == cudaSuccess) *launches += 1;
   return e;
 }

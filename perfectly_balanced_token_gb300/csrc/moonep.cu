@@ -19,6 +19,14 @@ cudaError_t launch_grouped_gemm(const Dims&, const PlanPtrs&, const void*, const
 cudaError_t launch_combine(const Dims&, const PlanPtrs&, const void*, const float*, void*,
                            cudaStream_t, int*);
 cudaError_t launch_reduce(const Dims&, const PlanPtrs&, float*, float*, cudaStream_t, int*);
+cudaError_t launch_grouped_gemm_dx(const Dims&, const PlanPtrs&, const void*, const void*, const void*,
+                                   void*, cudaStream_t, int*);
+cudaError_t launch_grouped_gemm_dw(const Dims&, const PlanPtrs&, const void*, const void*, float*,
+                                   float*, cudaStream_t, int*);
+cudaError_t launch_combine_backward(const Dims&, const PlanPtrs&, const void*, const float*,
+                                    const void*, void*, float*, cudaStream_t, int*);
+cudaError_t launch_dispatch_backward(const Dims&, const PlanPtrs&, const void*, void*, cudaStream_t,
+                                     int*);
 cudaError_t launch_wait_selftest(int32_t*, uint32_t, int32_t*, cudaStream_t, int*);
 
 static std::atomic<uint64_t> g_launches{0};
@@ -51,6 +59,7 @@ static int check_dims(const moonep_dims* in, Dims* d) {
   const int64_t mt = (N + d->tile_m - 1) / d->tile_m + (int64_t)x.R * groups;
   if (mt >= (int64_t(1) << 31)) return MOONEP_ERR_SHAPE;
   d->max_mtiles = (int)mt;
+  d->max_groups = (int)std::min<int64_t>((int64_t)x.R * groups, int64_t(1) << 30);
   return MOONEP_OK;
 }
 
@@ -90,6 +99,8 @@ static Layout make_layout(const Dims& d) {
   L.red_list = take(4 * E);
   L.rank_tiles = take(4 * (R + 1));
   p.mtiles = take(sizeof(MTile) * (size_t)d.max_mtiles);
+  L.rank_groups = take(4 * (R + 1));
+  p.groups = take(sizeof(MTile) * (size_t)d.max_groups);
   p.total_bytes = off;
   p.nchunk = d.nchunk;
   p.max_mtiles = d.max_mtiles;
@@ -125,6 +136,8 @@ static PlanPtrs resolve(const Layout& L, void* ws) {
   q.red_list = (int32_t*)(b + L.red_list);
   q.rank_tiles = (int32_t*)(b + L.rank_tiles);
   q.mtiles = (MTile*)(b + p.mtiles);
+  q.rank_groups = (int32_t*)(b + L.rank_groups);
+  q.groups = (MTile*)(b + p.groups);
   return q;
 }
 
@@ -254,6 +267,61 @@ int moonep_reduce_grad(const moonep_dims* dims, void* plan_ws, float* g_home, fl
   return finish(e, n);
 }
 
+int moonep_combine_backward(const moonep_dims* dims, void* plan_ws, const uint16_t* y,
+                            const float* gates, const uint16_t* d_out, uint16_t* d_y,
+                            float* d_gates, void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(y);
+  MOONEP_NEED(gates);
+  MOONEP_NEED(d_out);
+  MOONEP_NEED(d_y);
+  MOONEP_NEED(d_gates);
+  if (d.K > 128 || d.Hp > 8192) return MOONEP_ERR_SHAPE;
+  int n = 0;
+  const cudaError_t e = launch_combine_backward(d, P, y, gates, d_out, d_y, d_gates,
+                                                (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
+
+int moonep_grouped_gemm_dx(const moonep_dims* dims, void* plan_ws, const uint16_t* d_y,
+                           const uint16_t* w_home, const uint16_t* w_slot, uint16_t* d_recv,
+                           void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(d_y);
+  MOONEP_NEED(w_home);
+  MOONEP_NEED(d_recv);
+  if (d.B > 0) MOONEP_NEED(w_slot);
+  int n = 0;
+  const cudaError_t e = launch_grouped_gemm_dx(d, P, d_y, w_home, w_slot, d_recv,
+                                               (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
+
+int moonep_grouped_gemm_dw(const moonep_dims* dims, void* plan_ws, const uint16_t* recv,
+                           const uint16_t* d_y, float* g_home, float* g_slot, void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(recv);
+  MOONEP_NEED(d_y);
+  MOONEP_NEED(g_home);
+  if (d.B > 0) MOONEP_NEED(g_slot);
+  if (d.mode != 0) return MOONEP_ERR_ARG;       // gradients exist in training only
+  if (d.H % 128 != 0) return MOONEP_ERR_SHAPE;  // 128-row tiles of H
+  int n = 0;
+  const cudaError_t e = launch_grouped_gemm_dw(d, P, recv, d_y, g_home, g_slot,
+                                               (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
+
+int moonep_dispatch_backward(const moonep_dims* dims, void* plan_ws, const uint16_t* d_recv,
+                             uint16_t* d_x, void* stream) {
+  MOONEP_PROLOGUE(dims, plan_ws);
+  MOONEP_NEED(d_recv);
+  MOONEP_NEED(d_x);
+  int n = 0;
+  const cudaError_t e = launch_dispatch_backward(d, P, d_recv, d_x, (cudaStream_t)stream, &n);
+  return finish(e, n);
+}
+
 int moonep_read_status(const moonep_dims* dims, const void* plan_ws, int32_t* host_status,
                        void* stream) {
   MOONEP_PROLOGUE(dims, plan_ws);
@@ -344,7 +412,7 @@ static int noalloc_base(void** out) {
 
 // Offsets of the planner's internal tables inside the static array.
 struct NoAllocLayout {
-  size_t counts, pieces, piece_n, piece_base, home_base, rank_tiles, total;
+  size_t counts, pieces, piece_n, piece_base, home_base, rank_tiles, rank_groups, total;
 };
 
 static NoAllocLayout noalloc_layout(const Dims& d) {
@@ -362,6 +430,7 @@ static NoAllocLayout noalloc_layout(const Dims& d) {
   L.piece_base = take(4 * E * R);
   L.home_base = take(4 * E);
   L.rank_tiles = take(4 * (R + 1));
+  L.rank_groups = take(4 * (R + 1));
   L.total = off;
   return L;
 }
@@ -385,6 +454,7 @@ extern "C" int moonep_plan_noalloc(const moonep_dims* dims, const int32_t* topk_
   Q.piece_base = (int32_t*)(b + S.piece_base);
   Q.home_base = (int32_t*)(b + S.home_base);
   Q.rank_tiles = (int32_t*)(b + S.rank_tiles);
+  Q.rank_groups = (int32_t*)(b + S.rank_groups);
   int n = 0;
   const cudaError_t e = launch_plan(d, topk_idx, Q, (cudaStream_t)stream, &n);
   return finish(e, n);

@@ -198,6 +198,124 @@ k_combine(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restri
 }
 
 // ---------------------------------------------------------------------------
+// backward of combine: for out[t] = sum_k g[t,k] Y[dst(t,k)],
+//   dY[dst(t,k)] = bf16(g[t,k] * dout[t])   and   dg[t,k] = <Y[dst(t,k)], dout[t]>
+// (fp32 products and sums).  One CTA per token; each thread keeps its slice of
+// the dout row in registers; the K dot products are block reductions.
+// ---------------------------------------------------------------------------
+constexpr int kBwdMaxK = 128;
+
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads)
+k_combine_bwd(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restrict__ gates,
+              const uint4* __restrict__ dout, uint4* __restrict__ dy, float* __restrict__ dgates) {
+  __shared__ float part[kRowThreads / 32][kBwdMaxK];
+  if (plan_failed(p.status)) return;
+  const int hv = d.Hp / 8;
+  const int ntok = d.R * d.S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    float o[VPT][8];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int a = threadIdx.x + i * kRowThreads;
+      if (a < hv) {
+        const uint4 v = __ldcs(dout + (size_t)t * hv + a);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(h[j]);
+          o[i][2 * j] = f.x;
+          o[i][2 * j + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[i][j] = 0.f;
+      }
+    }
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    const float* gt = gates + (size_t)t * d.K;
+    for (int k = 0; k < d.K; ++k) {
+      const size_t row = (size_t)__ldg(dt + k);
+      const float g = __ldg(gt + k);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int a = threadIdx.x + i * kRowThreads;
+        if (a < hv) {
+          const uint4 v = __ldcs(y + row * hv + a);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+          uint4 w;
+          __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            dot = fmaf(f.x, o[i][2 * j], dot);
+            dot = fmaf(f.y, o[i][2 * j + 1], dot);
+            hw[j] = __floats2bfloat162_rn(g * o[i][2 * j], g * o[i][2 * j + 1]);
+          }
+          __stcs(dy + row * hv + a, w);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) part[warp][k] = dot;
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < d.K; k += kRowThreads) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRowThreads / 32; ++w) sum += part[w][k];
+      dgates[(size_t)t * d.K + k] = sum;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward of dispatch: dx[t] = bf16( sum over k ascending of dRecv[dst(t,k)] )
+// (fp32 sums), the adjoint of writing x[t] to every destination row.
+// ---------------------------------------------------------------------------
+template <int KC>
+__global__ void __launch_bounds__(kRowThreads)
+k_dispatch_bwd(Dims d, PlanPtrs p, const uint4* __restrict__ drecv, uint4* __restrict__ dx) {
+  if (plan_failed(p.status)) return;
+  const int hv = d.H / 8;
+  const int ntok = d.R * d.S;
+  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
+    const int32_t* dt = p.dst + (size_t)t * d.K;
+    for (int a = threadIdx.x; a < hv; a += kRowThreads) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int k0 = 0; k0 < d.K; k0 += KC) {
+        uint4 v[KC];
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+          if (k0 + k < d.K) v[k] = __ldcs(drecv + (size_t)__ldg(dt + k0 + k) * hv + a);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          if (k0 + k < d.K) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __bfloat1622float2(h[j]);
+              acc[2 * j] += f.x;
+              acc[2 * j + 1] += f.y;
+            }
+          }
+        }
+      }
+      uint4 o;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      __stcs(dx + (size_t)t * hv + a, o);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // reduce_grad: g_home[e] += g_slot[s] for the slots s holding e (ascending),
 // then g_slot[s] = 0 ("Moonshot AI 开源 MoonEP", contract paragraph)
 //
@@ -337,6 +455,37 @@ cudaError_t launch_combine(const Dims& d, const PlanPtrs& p, const void* y, cons
     k_combine<8><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)y, gates, (uint4*)out);
   else
     k_combine<4><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)y, gates, (uint4*)out);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_backward(const Dims& d, const PlanPtrs& p, const void* y,
+                                    const float* gates, const void* dout, void* dy, float* dgates,
+                                    cudaStream_t st, int* launches) {
+  const int hv = d.Hp / 8;
+  const int vpt = (hv + kRowThreads - 1) / kRowThreads;
+  const int ntok = d.R * d.S;
+  const int grid = min(ntok, sm_count() * 16);
+  const uint4 *ys = (const uint4*)y, *os = (const uint4*)dout;
+  uint4* dys = (uint4*)dy;
+  if (d.K > kBwdMaxK) return cudaErrorInvalidValue;
+  if (vpt <= 1) k_combine_bwd<1><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 2) k_combine_bwd<2><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 4) k_combine_bwd<4><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 8) k_combine_bwd<8><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else return cudaErrorInvalidValue;
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_backward(const Dims& d, const PlanPtrs& p, const void* drecv, void* dx,
+                                     cudaStream_t st, int* launches) {
+  const int ntok = d.R * d.S;
+  const int grid = min(ntok, sm_count() * 16);
+  if (d.K >= 8)
+    k_dispatch_bwd<8><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)drecv, (uint4*)dx);
+  else
+    k_dispatch_bwd<4><<<grid, kRowThreads, 0, st>>>(d, p, (const uint4*)drecv, (uint4*)dx);
   *launches += 1;
   return cudaGetLastError();
 }

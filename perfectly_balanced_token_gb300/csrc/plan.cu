@@ -102,7 +102,8 @@ k_plan(Dims d, PlanPtrs p) {
   int32_t* sState = sLoad + d.R;    // [R]
   int32_t* sCur = sState + d.R;     // [R]
   int32_t* sTiles = sCur + d.R;     // [R]
-  int32_t* sPieceN = sTiles + d.R;  // [E] pieces per expert so far
+  int32_t* sGroups = sTiles + d.R;  // [R] non-empty weight-row groups per rank
+  int32_t* sPieceN = sGroups + d.R; // [E] pieces per expert so far
   if (plan_failed(p.status)) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int EB = d.E + d.B;
@@ -130,6 +131,7 @@ k_plan(Dims d, PlanPtrs p) {
     p.n_recv[h] = 0;
     p.src[h] = -1;
     sTiles[h] = 0;
+    sGroups[h] = 0;
   }
   for (int i = tid; i < 3 * max(d.R - 1, 1); i += nt) p.fills[i] = -1;
   __syncthreads();
@@ -190,6 +192,7 @@ k_plan(Dims d, PlanPtrs p) {
         sPieceN[e] = pi + 1;
         p.cu[(size_t)u * (EB + 1) + g + 1] = t;
         sTiles[u] += (t + d.tile_m - 1) / d.tile_m;
+        sGroups[u] += 1;
         sMig[e] += t;
         need -= t;
         ++j;
@@ -221,6 +224,7 @@ k_plan(Dims d, PlanPtrs p) {
     const int h = e / d.L;
     p.cu[(size_t)h * (EB + 1) + e + 1] = k;
     atomicAdd(&sTiles[h], (k + d.tile_m - 1) / d.tile_m);
+    if (k > 0) atomicAdd(&sGroups[h], 1);
   }
   // reduce lists: the slots holding e in ascending (u, j)
   for (int s = tid; s < d.R * d.B; s += nt) {
@@ -269,6 +273,14 @@ k_plan(Dims d, PlanPtrs p) {
       p.rank_tiles[d.R] = run;
       p.counters[MOONEP_CNT_MTILES] = run;
       if (run > d.max_mtiles) set_error(p.status, MOONEP_ERR_INTERNAL);
+      run = 0;
+      for (int h = 0; h < d.R; ++h) {
+        p.rank_groups[h] = run;
+        run += sGroups[h];
+      }
+      p.rank_groups[d.R] = run;
+      p.counters[MOONEP_CNT_GROUPS] = run;
+      if (run > d.max_groups) set_error(p.status, MOONEP_ERR_INTERNAL);
     }
   }
 }
@@ -278,34 +290,37 @@ k_plan(Dims d, PlanPtrs p) {
 //    grid R, 1024 threads
 // ---------------------------------------------------------------------------
 template <int NT>
-__device__ __forceinline__ void block_scan2(int& a, int& b, int* sa, int* sb) {
-  // inclusive block scan of two ints; sa/sb hold NT/32 partials each
+__device__ __forceinline__ void block_scan3(int& a, int& b, int& c, int* sa, int* sb, int* sc) {
+  // inclusive block scan of three ints; sa/sb/sc hold NT/32 partials each
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int ya = __shfl_up_sync(0xffffffffu, a, o);
     const int yb = __shfl_up_sync(0xffffffffu, b, o);
-    if (lane >= o) { a += ya; b += yb; }
+    const int yc = __shfl_up_sync(0xffffffffu, c, o);
+    if (lane >= o) { a += ya; b += yb; c += yc; }
   }
-  if (lane == 31) { sa[warp] = a; sb[warp] = b; }
+  if (lane == 31) { sa[warp] = a; sb[warp] = b; sc[warp] = c; }
   __syncthreads();
   if (warp == 0) {
     int xa = lane < NT / 32 ? sa[lane] : 0, xb = lane < NT / 32 ? sb[lane] : 0;
+    int xc = lane < NT / 32 ? sc[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int ya = __shfl_up_sync(0xffffffffu, xa, o);
       const int yb = __shfl_up_sync(0xffffffffu, xb, o);
-      if (lane >= o) { xa += ya; xb += yb; }
+      const int yc = __shfl_up_sync(0xffffffffu, xc, o);
+      if (lane >= o) { xa += ya; xb += yb; xc += yc; }
     }
-    if (lane < NT / 32) { sa[lane] = xa; sb[lane] = xb; }
+    if (lane < NT / 32) { sa[lane] = xa; sb[lane] = xb; sc[lane] = xc; }
   }
   __syncthreads();
-  if (warp > 0) { a += sa[warp - 1]; b += sb[warp - 1]; }
+  if (warp > 0) { a += sa[warp - 1]; b += sb[warp - 1]; c += sc[warp - 1]; }
 }
 
 __global__ void __launch_bounds__(1024)
 k_tables(Dims d, PlanPtrs p) {
-  __shared__ int sa[32], sb[32];
+  __shared__ int sa[32], sb[32], sc[32];
   if (plan_failed(p.status)) return;
   const int u = blockIdx.x, tid = threadIdx.x;
   const int EB = d.E + d.B;
@@ -314,16 +329,17 @@ k_tables(Dims d, PlanPtrs p) {
   const int per = (EB + 1023) / 1024;
   const int g0 = min(EB, tid * per), g1 = min(EB, g0 + per);
   int rows_local[8];
-  int rsum = 0, tsum = 0;
+  int rsum = 0, tsum = 0, gsum = 0;
   for (int g = g0, i = 0; g < g1; ++g, ++i) {
     const int rows = cu[g + 1];
     if (i < 8) rows_local[i] = rows;
     rsum += rows;
     tsum += (rows + d.tile_m - 1) / d.tile_m;
+    gsum += rows > 0;
   }
-  int ra = rsum, tb = tsum;
-  block_scan2<1024>(ra, tb, sa, sb);
-  int row = ra - rsum, tile = tb - tsum + p.rank_tiles[u];
+  int ra = rsum, tb = tsum, gc = gsum;
+  block_scan3<1024>(ra, tb, gc, sa, sb, sc);
+  int row = ra - rsum, tile = tb - tsum + p.rank_tiles[u], grp = gc - gsum + p.rank_groups[u];
   __syncthreads();  // every thread has read its rows before they are replaced
   for (int g = g0, i = 0; g < g1; ++g, ++i) {
     const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 5 for E <= 4096
@@ -332,6 +348,7 @@ k_tables(Dims d, PlanPtrs p) {
     for (int m = 0; m * d.tile_m < rows; ++m) {
       p.mtiles[tile++] = MTile{u * d.C + row + m * d.tile_m, min(d.tile_m, rows - m * d.tile_m), wsel, u};
     }
+    if (rows > 0) p.groups[grp++] = MTile{u * d.C + row, rows, wsel, u};
     row += rows;
   }
   if (tid == 1023) cu[EB] = row;
@@ -432,7 +449,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     if (err != cudaSuccess) return err;
   }
   k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
-  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 4 * d.R);
+  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 5 * d.R);
   if (plan_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;

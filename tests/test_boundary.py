@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 15, names
+    assert len(names) == 19, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -98,6 +98,14 @@ def test_bad_pointers_rejected_before_launch(lib):
     assert lib.moonep_reduce_grad(D, ws, ok, None, None) == _lib.ERR_ARG
     assert lib.moonep_read_status(D, ws, None, None) == _lib.ERR_ARG
     assert lib.moonep_plan_export(D, ws, None, None) == _lib.ERR_ARG
+    assert lib.moonep_combine_backward(D, ws, ok, ok, ok, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_grouped_gemm_dx(D, ws, ok, ok, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_grouped_gemm_dw(D, ws, ok, ok, ok, None, None) == _lib.ERR_ARG
+    assert lib.moonep_dispatch_backward(D, ws, odd, ok, None) == _lib.ERR_ALIGN
+    infer = mx.dims(4, 8, 2, 2, 16, 128, 128, 1)
+    assert lib.moonep_grouped_gemm_dw(ctypes.byref(infer), ws, ok, ok, ok, ok, None) == _lib.ERR_ARG
+    h64 = mx.dims(4, 8, 2, 2, 16, 64, 128, 0)
+    assert lib.moonep_grouped_gemm_dw(ctypes.byref(h64), ws, ok, ok, ok, ok, None) == _lib.ERR_SHAPE
     bad = mx.dims(4, 8, 1, 2, 16, 64, 128, 0)
     assert lib.moonep_plan(ctypes.byref(bad), ok, ws, None) == _lib.ERR_SLOTS
     assert lib.moonep_plan(None, ok, ws, None) == _lib.ERR_ARG

@@ -46,6 +46,8 @@ def _regions(ws: mx.PlanWorkspace, n_mtiles: int):
     out = {f: (getattr(lay, f), ends[f]) for f in OUTPUT_TABLES}
     out["reduce"] = (lay.reduce, lay.reduce + _a256(4 * d.E * d.R) + 2 * _a256(4 * d.E))
     out["mtiles"] = (lay.mtiles, lay.mtiles + 16 * n_mtiles)
+    n_groups = int(ws.view("counters", (8,))[6])
+    out["groups"] = (lay.groups, lay.groups + 16 * n_groups)
     return out
 
 
