@@ -225,22 +225,39 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()  # before the warm-up, so nvidia-smi's start-up is over by the timed region
 
-    def time_policy(policy, warmup, steps):
+    bwd = {}  # backward buffers, allocated only when the training step is timed
+
+    def time_policy(policy, warmup, steps, training=False):
         """Warm up eagerly, capture one CUDA graph per (routing, segment), then
-        time `steps` steps of graph replays with events between segments."""
+        time `steps` steps of graph replays with events between segments.  The
+        forward step is plan .. combine + reduce_grad; a training step inserts
+        the backward (combine backward, the two GEMM gradients, dispatch
+        backward) before reduce_grad."""
         d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy)
         ws = mx.PlanWorkspace(d, device=dev)
 
         def calls(j):
             # stream=None: the current stream (the capture stream while capturing)
-            return (
+            fwd = (
                 lambda: mx.moonep_plan(d, idx[j], ws.buf),
                 lambda: mx.moonep_prefetch_weights(d, ws.buf, w_home, w_slot),
                 lambda: mx.moonep_dispatch(d, ws.buf, x, recv),
                 lambda: mx.moonep_grouped_gemm(d, ws.buf, recv, w_home, w_slot, y),
                 lambda: mx.moonep_combine(d, ws.buf, y, gates[j], out),
-                lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot),
             )
+            back = ()
+            if training:
+                b = bwd
+                back = (
+                    lambda: mx.moonep_combine_backward(d, ws.buf, y, gates[j], b["dout"], b["dy"],
+                                                       b["dgates"]),
+                    lambda: mx.moonep_grouped_gemm_dx(d, ws.buf, b["dy"], w_home, w_slot,
+                                                      b["drecv"]),
+                    lambda: mx.moonep_grouped_gemm_dw(d, ws.buf, recv, b["dy"], g_home, g_slot),
+                    lambda: mx.moonep_dispatch_backward(d, ws.buf, b["drecv"], b["dx"]),
+                )
+            return fwd + back + (lambda: mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot),)
+        nseg = len(calls(0))
 
         for i in range(warmup):
             for c in calls(i % len(sweep)):
@@ -280,7 +297,7 @@ def run_ours(args):
                 g.replay()
         torch.cuda.synchronize()
 
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(steps)]
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
@@ -290,10 +307,10 @@ def run_ours(args):
         for i in range(steps):
             j = i % len(sweep)
             flush.fill_(float(i))  # evict L2 between steps (not inside a step's events)
-            for k in range(6):
+            for k in range(nseg):
                 evs[i][k].record()
                 graphs[j][k].replay()
-            evs[i][6].record()
+            evs[i][nseg].record()
             launches += sum(graph_launches[j])
         torch.cuda.synchronize()
         t1 = time.time()
@@ -303,7 +320,7 @@ def run_ours(args):
         if status:
             raise RuntimeError(f"device status after the timed steps {status:#x}: "
                                f"{mx.status_string(status)}")
-        seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(6)]
+        seg = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(nseg)]
                         for i in range(steps)])  # ms
         return d, ws, seg, counters, launches, (t0, t1)
 
@@ -339,6 +356,30 @@ def run_ours(args):
                    "value": N * args.steps * world / (ms1 / 1e3),
                    "ms_per_step": ms1 / args.steps,
                    "sweep": per_maxvio(seg1, counters1)}
+
+    training = None
+    if not args.no_training:
+        bwd.update(
+            dout=syn.normal_bf16((w.R, w.S, w.Hp), 1.0, 5, dev).view(-1),
+            dy=torch.empty(N * w.Hp, dtype=torch.bfloat16, device=dev),
+            dgates=torch.empty(N, dtype=torch.float32, device=dev),
+            drecv=torch.empty(N * w.H, dtype=torch.bfloat16, device=dev),
+            dx=torch.empty(w.R * w.S * w.H, dtype=torch.bfloat16, device=dev))
+        _, _, segt, _, _, _ = time_policy(0, 1, args.steps, training=True)
+        tnames = names[:5] + ("combine_backward", "gemm_dx", "gemm_dw", "dispatch_backward",
+                              "reduce_grad")
+        mst = reduce_max(float(segt.sum()), world, dev)
+        bd = {n: float(segt[:, k].mean()) for k, n in enumerate(tnames)}
+        fl = 2.0 * N * w.H * w.Hp
+        training = {"step": "forward (plan .. combine) + combine backward + input-gradient GEMM "
+                            "+ weight-gradient GEMM + dispatch backward + reduce_grad",
+                    "value": N * args.steps * world / (mst / 1e3), "ms_per_step": mst / args.steps,
+                    "breakdown_ms": bd,
+                    "gemm_dx_tflops": fl / (bd["gemm_dx"] / 1e3) / 1e12,
+                    "gemm_dw_tflops": fl / (bd["gemm_dw"] / 1e3) / 1e12}
+        for b_ in list(bwd):
+            del bwd[b_]
+        torch.cuda.empty_cache()
 
     # e2e: host buffers through the same C ABI, copies inside the timed region
     e2e = None if args.no_e2e else run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot,
@@ -393,6 +434,7 @@ def run_ours(args):
         "step_ms": [float(v) for v in step_ms],
         "planner": "Theorem 1 construction, fixed tie-break (dims.policy = 0)",
         "planner_largest_first": policy1,
+        "training_step": training,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "pages":
         result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
@@ -548,6 +590,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-policy-sweep", action="store_true",
                     help="skip timing the largest-first planner policy")
+    ap.add_argument("--no-training", action="store_true",
+                    help="skip timing the training step (forward + backward)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pages",
                     help="pages = the headline configuration; the others are smaller cases "
                          "of the same kernels for profiling")

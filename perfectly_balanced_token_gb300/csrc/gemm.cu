@@ -599,25 +599,30 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 // boxes of 64(n) x 64(row)).  The reduction runs over the group's rows in
 // 64-row blocks; in the last block the rows past the group's end are zeroed
 // in shared memory before the MMAs.  Accumulators are double buffered in TMEM;
-// the epilogue adds them into G with fp32 read-modify-writes.
+// the epilogue stages them in shared memory and adds them into G with TMA
+// reduce-adds, so the read-modify-write happens in L2.
 template <int BN, int STAGES>
 struct GemmCfgDW {
   static constexpr int kABytes = kMmaM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kStageOut = 4096;            // 32 rows x 32 fp32, 128-byte swizzled
+  static constexpr int kOutBytes = 4 * 2 * kStageOut;  // 4 epilogue warps x 2 buffers
   static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
-  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
+  static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
 };
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
-           Dims d, PlanPtrs p, float* __restrict__ g_home, float* __restrict__ g_slot) {
+           const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gs,
+           Dims d, PlanPtrs p) {
   using Cfg = GemmCfgDW<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint8_t* out_stage = smem + STAGES * Cfg::kStageBytes;  // 1024-aligned
+  uint64_t* bars = (uint64_t*)(out_stage + Cfg::kOutBytes);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -649,6 +654,8 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_dy);
+    prefetch_tmap(&tm_gh);
+    prefetch_tmap(&tm_gs);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -750,10 +757,14 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
   } else {
     // ---------------- epilogue (warps 2..5): G += accumulator ----------------
+    // Each warp owns 32 rows of the tile.  A 32 x 32 fp32 chunk is drained from
+    // TMEM into one of two swizzled staging buffers and added into G by a TMA
+    // reduce (the read-modify-write happens in L2); a buffer is reused once the
+    // reduce that read it is done.
     const int q = warp & 3;
-    int acc = 0;
+    uint8_t* my_stage = out_stage + (size_t)(warp - 2) * 2 * Cfg::kStageOut;
+    int acc = 0, chunk = 0;
     uint32_t acc_phase = 0;
-    const size_t hh = (size_t)d.H * d.Hp;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const MTile grp = p.groups[t / per_group];
       const int m0 = ((t % per_group) / NT) * kMmaM;
@@ -767,36 +778,31 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         break;
       }
       tc_fence_after();
-      float* gbase = grp.wsel >= 0 ? g_home + (size_t)grp.wsel * hh
-                                   : g_slot + (size_t)(-1 - grp.wsel) * hh;
-      float* grow = gbase + (size_t)(m0 + q * 32 + lane) * d.Hp + n0;
+      const CUtensorMap* gmap = grp.wsel >= 0 ? &tm_gh : &tm_gs;
+      const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0 + q * 32;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; c += 2) {
-        float4 g0[8], g1[8];
-        float4* p0 = reinterpret_cast<float4*>(grow + c * 32);
-        float4* p1 = reinterpret_cast<float4*>(grow + (c + 1) * 32);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          g0[v] = p0[v];
-          g1[v] = p1[v];
-        }
-        uint32_t r0[32], r1[32];
-        tmem_ld_x32(tbase + c * 32, r0);
-        tmem_ld_x32(tbase + (c + 1) * 32, r1);
+      for (int c = 0; c < BN / 32; ++c, ++chunk) {
+        uint8_t* buf = my_stage + (chunk & 1) * Cfg::kStageOut;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld_x32(tbase + c * 32, r);
         tmem_ld_wait();
+        // row `lane`, 16-byte chunk j stored at chunk j ^ (lane % 8): 128-byte swizzle
+        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          g0[v].x += __uint_as_float(r0[4 * v + 0]);
-          g0[v].y += __uint_as_float(r0[4 * v + 1]);
-          g0[v].z += __uint_as_float(r0[4 * v + 2]);
-          g0[v].w += __uint_as_float(r0[4 * v + 3]);
-          g1[v].x += __uint_as_float(r1[4 * v + 0]);
-          g1[v].y += __uint_as_float(r1[4 * v + 1]);
-          g1[v].z += __uint_as_float(r1[4 * v + 2]);
-          g1[v].w += __uint_as_float(r1[4 * v + 3]);
-          p0[v] = g0[v];
-          p1[v] = g1[v];
+        for (int j = 0; j < 8; ++j)
+          row[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile(
+              "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+              " [%0, {%1, %2}], [%3];" ::"l"((uint64_t)gmap),
+              "r"(n0 + c * 32), "r"(grow), "r"(smem_u32(buf))
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
       }
       tc_fence_before();
@@ -804,6 +810,8 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (lane == 0) mbar_arrive(tempty(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -867,6 +875,19 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   cuuint32_t box[2] = {64, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D fp32 tensor [outer][inner] with a 32 x 32 box, 128-byte swizzle (TMA reduce target).
+static bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim, gstride, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -955,22 +976,27 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const PlanPtrs& p, const void*
 cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void* recv,
                                    const void* dy, float* g_home, float* g_slot, cudaStream_t st,
                                    int* launches) {
-  CUtensorMap tx, tdy;
+  CUtensorMap tx, tdy, tgh, tgs;
   if (!encode_2d(&tx, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
   if (!encode_2d(&tdy, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
+  if (!encode_2d_f32(&tgh, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H)) return cudaErrorInvalidValue;
+  const bool slots = g_slot != nullptr && d.B > 0;
+  if (!encode_2d_f32(&tgs, slots ? g_slot : g_home, (uint64_t)d.Hp,
+                     slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H))
+    return cudaErrorInvalidValue;
   const int bn = pick_bn(d.Hp);
   const long long max_items = (long long)d.max_groups * (d.H / kMmaM) * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_items));
   cudaError_t e;
   if (bn == 256) {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+    e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, tgh, tgs, d, p);
   } else if (bn == 128) {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<128, 6>>(k_ggemm_dw<128, 6>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+    e = launch_cfg<GemmCfgDW<128, 5>>(k_ggemm_dw<128, 5>, set, grid, st, tx, tdy, tgh, tgs, d, p);
   } else {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<64, 8>>(k_ggemm_dw<64, 8>, set, grid, st, tx, tdy, d, p, g_home, g_slot);
+    e = launch_cfg<GemmCfgDW<64, 7>>(k_ggemm_dw<64, 7>, set, grid, st, tx, tdy, tgh, tgs, d, p);
   }
   if (e == cudaSuccess) *launches += 1;
   return e;

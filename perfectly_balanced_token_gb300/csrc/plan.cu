@@ -100,8 +100,7 @@ k_plan(Dims d, PlanPtrs p) {
   int32_t* sMig = sT + d.E;         // [E]
   int32_t* sLoad = sMig + d.E;      // [R]
   int32_t* sState = sLoad + d.R;    // [R]
-  int32_t* sCur = sState + d.R;     // [R]
-  int32_t* sTiles = sCur + d.R;     // [R]
+  int32_t* sTiles = sState + d.R;   // [R]
   int32_t* sGroups = sTiles + d.R;  // [R] non-empty weight-row groups per rank
   int32_t* sPieceN = sGroups + d.R; // [E] pieces per expert so far
   if (plan_failed(p.status)) return;
@@ -113,11 +112,18 @@ k_plan(Dims d, PlanPtrs p) {
   for (int e = tid; e < d.E; e += nt) {
     int run = 0;
     int32_t* c = p.counts + e;
-#pragma unroll 8
-    for (int i = 0; i < rc; ++i) {
-      const int v = c[(size_t)i * d.E];
-      c[(size_t)i * d.E] = run;
-      run += v;
+    // 16 loads in flight before their stores: a load after a store to the same
+    // array would otherwise wait for the previous one
+    constexpr int kBatch = 16;
+    for (int i0 = 0; i0 < rc; i0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = (i0 + j < rc) ? c[(size_t)(i0 + j) * d.E] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (i0 + j < rc) c[(size_t)(i0 + j) * d.E] = run;
+        run += v[j];
+      }
     }
     sT[e] = run;
     p.T[e] = run;
@@ -141,77 +147,128 @@ k_plan(Dims d, PlanPtrs p) {
     sLoad[h] = s;
     p.load[h] = s;
     sState[h] = s < d.C ? kUnder : (s > d.C ? kOver : kBalanced);
-    sCur[h] = (h + 1) * d.L - 1;
   }
   __syncthreads();
 
-  // the fills, sequential by construction (at most R-1 of them)
-  if (tid == 0) {
+  // the fills, sequential by construction (at most R-1 of them); warp 0 runs
+  // them, each decision made with ballots / shuffles so all lanes agree
+  if (tid < 32) {
+    const int lane = tid;
+    const unsigned full = 0xffffffffu;
     int nfill = 0;
     bool ok = true;
+    // record one migrated range: ordinals [left - t, left) of expert e go to
+    // u as its j-th acquired expert (a slot, or the home row when j >= B)
+    auto emit = [&](int u, int e, int left, int t, int j) -> bool {
+      const int g = (j < d.B) ? d.E + j : e;
+      if (j < d.B) p.slot_expert[u * d.B + j] = e;
+      const int pi = sPieceN[e];
+      if (pi >= d.R) return false;
+      p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
+      sPieceN[e] = pi + 1;
+      p.cu[(size_t)u * (EB + 1) + g + 1] = t;
+      atomicAdd(&sTiles[u], (t + d.tile_m - 1) / d.tile_m);
+      atomicAdd(&sGroups[u], 1);
+      sMig[e] += t;
+      return true;
+    };
     while (ok) {
       int u = -1, o = -1;
-      if (d.policy == 1) {  // largest deficit from largest surplus, ties to the smallest id
-        int best_def = 0, best_sur = 0;
-        for (int h = 0; h < d.R; ++h) {
-          if (sState[h] == kUnder && d.C - sLoad[h] > best_def) { best_def = d.C - sLoad[h]; u = h; }
-          if (sState[h] == kOver && sLoad[h] - d.C > best_sur) { best_sur = sLoad[h] - d.C; o = h; }
+      if (d.policy == 1) {
+        // largest deficit / largest surplus, ties to the smallest id: per-lane
+        // best over a strided subset, then a warp argmax
+        int bd = 0, bs = 0;
+        for (int h = lane; h < d.R; h += 32) {
+          const int st = sState[h], ld = sLoad[h];
+          if (st == kUnder && d.C - ld > bd) { bd = d.C - ld; u = h; }
+          if (st == kOver && ld - d.C > bs) { bs = ld - d.C; o = h; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const int od = __shfl_xor_sync(full, bd, off), ou = __shfl_xor_sync(full, u, off);
+          if (ou >= 0 && (u < 0 || od > bd || (od == bd && ou < u))) { bd = od; u = ou; }
+          const int os = __shfl_xor_sync(full, bs, off), oo = __shfl_xor_sync(full, o, off);
+          if (oo >= 0 && (o < 0 || os > bs || (os == bs && oo < o))) { bs = os; o = oo; }
         }
       } else {
-        for (int h = 0; h < d.R && (u < 0 || o < 0); ++h) {
-          if (u < 0 && sState[h] == kUnder) u = h;
-          if (o < 0 && sState[h] == kOver) o = h;
+        // the smallest-id underloaded and overloaded ranks
+        for (int h0 = 0; h0 < d.R && (u < 0 || o < 0); h0 += 32) {
+          const int h = h0 + lane;
+          const int st = h < d.R ? sState[h] : kBalanced;
+          const unsigned mu = __ballot_sync(full, st == kUnder), mo = __ballot_sync(full, st == kOver);
+          if (u < 0 && mu) u = h0 + __ffs(mu) - 1;
+          if (o < 0 && mo) o = h0 + __ffs(mo) - 1;
         }
       }
       if (u < 0) break;
       if (o < 0 || nfill >= d.R - 1) { ok = false; break; }
       const int dcopies = d.C - sLoad[u];
       int need = dcopies, j = 0;
-      while (need > 0) {
-        int e, left;
-        if (d.policy == 1) {  // the donor expert with the most copies left, ties to the highest id
-          e = -1;
-          left = 0;
-          for (int c = o * d.L; c < (o + 1) * d.L; ++c) {
+      if (d.policy == 1) {
+        // repeatedly the donor expert with the most copies left, ties to the highest id
+        while (need > 0 && ok) {
+          int bl = 0, be = -1;
+          for (int c = o * d.L + lane; c < (o + 1) * d.L; c += 32) {
             const int lc = sT[c] - sMig[c];
-            if (lc > 0 && lc >= left) { left = lc; e = c; }
+            if (lc > 0 && lc >= bl) { bl = lc; be = c; }
           }
-          if (e < 0) { ok = false; break; }
-        } else {
-          e = sCur[o];
-          if (e < o * d.L) { ok = false; break; }
-          left = sT[e] - sMig[e];
-          if (left == 0) { sCur[o] = e - 1; continue; }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const int ol = __shfl_xor_sync(full, bl, off), oe = __shfl_xor_sync(full, be, off);
+            if (ol > bl || (ol == bl && oe > be)) { bl = ol; be = oe; }
+          }
+          if (be < 0) { ok = false; break; }
+          const int t = min(bl, need);
+          bool good = true;
+          if (lane == 0) good = emit(u, be, bl, t, j);
+          ok = __shfl_sync(full, good, 0);
+          __syncwarp();
+          need -= t;
+          ++j;
         }
-        const int t = min(left, need);
-        const int g = (j < d.B) ? d.E + j : e;  // slot, or inference overflow row
-        if (j < d.B) p.slot_expert[u * d.B + j] = e;
-        const int pi = sPieceN[e];
-        if (pi >= d.R) { ok = false; break; }
-        p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
-        sPieceN[e] = pi + 1;
-        p.cu[(size_t)u * (EB + 1) + g + 1] = t;
-        sTiles[u] += (t + d.tile_m - 1) / d.tile_m;
-        sGroups[u] += 1;
-        sMig[e] += t;
-        need -= t;
-        ++j;
+      } else {
+        // o's experts in descending id, 32 at a time: each takes min(left,
+        // what is still needed after the higher ones)
+        for (int top = (o + 1) * d.L - 1; top >= o * d.L && need > 0 && ok; top -= 32) {
+          const int e = top - lane;
+          const int left = (e >= o * d.L) ? sT[e] - sMig[e] : 0;
+          int incl = left;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(full, incl, off);
+            if (lane >= off) incl += v;
+          }
+          const int t = max(0, min(left, need - (incl - left)));
+          const unsigned mt = __ballot_sync(full, t > 0);
+          bool good = true;
+          if (t > 0) good = emit(u, e, left, t, j + __popc(mt & ((1u << lane) - 1u)));
+          ok = __all_sync(full, good);
+          __syncwarp();
+          j += __popc(mt);
+          need -= min(need, __shfl_sync(full, incl, 31));
+        }
+        if (need > 0) ok = false;  // o ran out of copies (cannot happen for an overloaded o)
       }
       if (!ok) break;
       if (d.mode == 0 && j > d.B) { ok = false; break; }
-      p.fills[3 * nfill + 0] = u;
-      p.fills[3 * nfill + 1] = o;
-      p.fills[3 * nfill + 2] = dcopies;
-      p.n_recv[u] = j;
-      p.src[u] = o;
+      if (lane == 0) {
+        p.fills[3 * nfill + 0] = u;
+        p.fills[3 * nfill + 1] = o;
+        p.fills[3 * nfill + 2] = dcopies;
+        p.n_recv[u] = j;
+        p.src[u] = o;
+        sLoad[u] = d.C;
+        sState[u] = kBalanced;
+        sLoad[o] -= dcopies;
+        sState[o] = sLoad[o] < d.C ? kUnder : (sLoad[o] > d.C ? kOver : kBalanced);
+      }
+      __syncwarp();
       ++nfill;
-      sLoad[u] = d.C;
-      sState[u] = kBalanced;
-      sLoad[o] -= dcopies;
-      sState[o] = sLoad[o] < d.C ? kUnder : (sLoad[o] > d.C ? kOver : kBalanced);
     }
-    if (!ok) set_error(p.status, MOONEP_ERR_INTERNAL);
-    p.counters[MOONEP_CNT_FILLS] = nfill;
+    if (lane == 0) {
+      if (!ok) set_error(p.status, MOONEP_ERR_INTERNAL);
+      p.counters[MOONEP_CNT_FILLS] = nfill;
+    }
   }
   __syncthreads();
   if (plan_failed(p.status)) return;
@@ -449,7 +506,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     if (err != cudaSuccess) return err;
   }
   k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
-  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 5 * d.R);
+  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 4 * d.R);
   if (plan_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;
