@@ -32,6 +32,12 @@ CASES = [  # H % 128 == 0 for the weight gradient
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.5, seed=7), 0),
     ("ragged-h256", W("ragged256", R=5, E=20, B=4, K=3, S=171, H=256, Hp=320),
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.3, seed=6), 0),
+    # ragged groups with several 256-wide column tiles in both directions, and
+    # an input gradient with 128-wide column tiles (H = 384)
+    ("ragged-h512", W("ragged512", R=4, E=12, B=3, K=3, S=500, H=512, Hp=512),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=11), 0),
+    ("ragged-h384", W("ragged384", R=4, E=12, B=3, K=3, S=400, H=384, Hp=512),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=12), 0),
 ]
 
 

@@ -55,6 +55,14 @@ CASES = [
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=2.5, seed=8)),
     ("m256-infer-b0", W("m256i", R=2, E=4, B=0, K=1, S=9000, H=64, Hp=128, mode=1),
      lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=2)),
+    # several 256-wide column tiles with ragged groups of a few 128-row tiles,
+    # groups mostly under one tile, and inference overflow
+    ("bn256-ragged", W("bn256r", R=4, E=12, B=3, K=3, S=700, H=192, Hp=512),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=9)),
+    ("bn256-small-groups", W("bn256s", R=8, E=64, B=8, K=2, S=200, H=64, Hp=512),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=0.8, seed=10)),
+    ("bn256-infer-overflow", W("bn256i", R=4, E=16, B=1, K=2, S=300, H=128, Hp=1024, mode=1),
+     lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=4)),
 ]
 
 
