@@ -17,8 +17,9 @@
 //    stage holds 2 A boxes and one B panel, so each byte of B fetched from L2
 //    feeds twice the MMA work of a single 128-row tile.  A tile whose group
 //    ends within its first half issues only the first half's MMAs.
-//  * warp 0: TMA producer (A boxes 64x128 K-major, B boxes 64x64 N-major, all
-//    128-byte swizzled) into a STAGES-deep shared-memory ring;
+//  * warp 0: TMA producer (A boxes 64x128 K-major; B as BN/64 panels of 64x64
+//    N-major fetched by one 3D box; all 128-byte swizzled) into a
+//    STAGES-deep shared-memory ring;
 //    warp 1: TMEM allocation and the single-thread tcgen05.mma issuer
 //    (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM);
 //    warps 2..5: epilogue, tcgen05.ld of an accumulator, bf16 rounding
@@ -119,6 +120,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)m),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -205,15 +219,15 @@ struct GemmShape {
 // B stage loads and descriptors for the two layouts of the weight operand.
 template <int BN, bool BKM>
 struct BOperand {
-  // N-major: BN/64 boxes of 64(n) x 64(k), 8 KiB apart; K-major: one box of
-  // 64(k) x BN(n) rows of 128 B.
+  // N-major: one box of BN/64 panels of 64(n) x 64(k), 8 KiB apart, from the
+  // weights viewed as [H'/64][rows][64] (one TMA request instead of BN/64);
+  // K-major: one box of 64(k) x BN(n) rows of 128 B.
   static __device__ __forceinline__ void load(uint32_t sb, const CUtensorMap* m, uint32_t bar,
                                               int n0, int k0, int wrow) {
     if (BKM) {
       tma_load_2d(sb, m, bar, k0, wrow + n0);
     } else {
-#pragma unroll
-      for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, m, bar, n0 + i * 64, wrow + k0);
+      tma_load_3d(sb, m, bar, 0, wrow + k0, n0 / 64);
     }
   }
   static __device__ __forceinline__ uint64_t desc(uint32_t sb, int k) {
@@ -595,20 +609,29 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 // folds into the home rows).  Work items are (group, 128-row tile of H, BN
 // column tile of H'), column tiles fastest, so the CTAs running together read
 // the same group's rows from L2.  Both operands are read N-major straight from
-// the row-major buffers: A = X^T (two 64(h) x 64(row) boxes), B = dY (BN/64
-// boxes of 64(n) x 64(row)).  The reduction runs over the group's rows in
-// 64-row blocks; in the last block the rows past the group's end are zeroed
-// in shared memory before the MMAs.  Accumulators are double buffered in TMEM;
-// the epilogue stages them in shared memory and adds them into G with TMA
-// reduce-adds, so the read-modify-write happens in L2.
+// the row-major buffers, each stage by two 3D boxes: A = X^T (2 panels of
+// 64(h) x 64(row)), B = dY (BN/64 panels of 64(n) x 64(row)).  The reduction
+// runs over the group's rows in 64-row blocks; in the last block the rows past
+// the group's end are zeroed in shared memory before the MMAs.  Accumulators
+// are double buffered in TMEM.  The four epilogue warps stage a 128 x 32 fp32
+// chunk together in shared memory and one thread adds it into G with a TMA
+// reduce-add, so the read-modify-write happens in L2.  Every G element gets
+// one add per launch, always a cold line: for groups long enough to hide it,
+// the producer asks L2 to prefetch the item's G tile when the item starts, so
+// the reduce-adds at its end find the lines resident.
+// The weight gradient prefetches a work item's G tile into L2 only when the
+// item reduces over at least this many 64-row blocks (measured: shorter items
+// leave too little time for the prefetch and only add DRAM traffic).
+constexpr int kDwPrefetchMinBlocks = 16;
+
 template <int BN, int STAGES>
 struct GemmCfgDW {
   static constexpr int kABytes = kMmaM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kStageOut = 4096;            // 32 rows x 32 fp32, 128-byte swizzled
-  static constexpr int kOutBytes = 4 * 2 * kStageOut;  // 4 epilogue warps x 2 buffers
+  static constexpr int kStageOut = 16384;           // 128 rows x 32 fp32, 128-byte swizzled
+  static constexpr int kOutBytes = 2 * kStageOut;      // 2 buffers shared by the 4 epilogue warps
   static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
   static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
 };
@@ -617,6 +640,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
            const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gs,
+           const __grid_constant__ CUtensorMap tm_ghp, const __grid_constant__ CUtensorMap tm_gsp,
            Dims d, PlanPtrs p) {
   using Cfg = GemmCfgDW<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -677,16 +701,16 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const int m0 = ((t % per_group) / NT) * kMmaM;
         const int n0 = (t % NT) * BN;
         const int KB = (grp.rows + kBK - 1) / kBK;
+        if (KB >= kDwPrefetchMinBlocks)
+          tma_prefetch_2d(grp.wsel >= 0 ? &tm_ghp : &tm_gsp, n0,
+                          (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           mbar_expect_tx(full(stage), Cfg::kStageBytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
           const int r0 = grp.row0 + kb * kBK;
-          tma_load_2d(sa, &tm_x, full(stage), m0, r0);
-          tma_load_2d(sa + 8192, &tm_x, full(stage), m0 + 64, r0);
-#pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sa + Cfg::kABytes + i * 8192, &tm_dy, full(stage), n0 + i * 64, r0);
+          tma_load_3d(sa, &tm_x, full(stage), 0, r0, m0 / 64);
+          tma_load_3d(sa + Cfg::kABytes, &tm_dy, full(stage), 0, r0, n0 / 64);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -762,15 +786,26 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // reduce (the read-modify-write happens in L2); a buffer is reused once the
     // reduce that read it is done.
     const int q = warp & 3;
-    uint8_t* my_stage = out_stage + (size_t)(warp - 2) * 2 * Cfg::kStageOut;
+    const bool issuer = (warp == 2 && lane == 0);
+    auto epi_bar = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    auto epi_all = [](bool pred) {
+      uint32_t r;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+          : "=r"(r)
+          : "r"((uint32_t)pred)
+          : "memory");
+      return r != 0;
+    };
     int acc = 0, chunk = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const MTile grp = p.groups[t / per_group];
       const int m0 = ((t % per_group) / NT) * kMmaM;
       const int n0 = (t % NT) * BN;
-      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
+      const bool okw = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!epi_all(okw)) {
         if (lane == 0) {
           *abort_flag = 1;
           set_error(p.status, MOONEP_ERR_TIMEOUT);
@@ -779,24 +814,24 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       }
       tc_fence_after();
       const CUtensorMap* gmap = grp.wsel >= 0 ? &tm_gh : &tm_gs;
-      const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0 + q * 32;
+      const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const int rr = q * 32 + lane;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c, ++chunk) {
-        uint8_t* buf = my_stage + (chunk & 1) * Cfg::kStageOut;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        __syncwarp();
+        uint8_t* buf = out_stage + (chunk & 1) * Cfg::kStageOut;
+        if (issuer) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        epi_bar();
         uint32_t r[32];
         tmem_ld_x32(tbase + c * 32, r);
         tmem_ld_wait();
-        // row `lane`, 16-byte chunk j stored at chunk j ^ (lane % 8): 128-byte swizzle
-        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+        uint4* row = reinterpret_cast<uint4*>(buf + rr * 128);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          row[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          row[j ^ (rr & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
+        epi_bar();
+        if (issuer) {
           asm volatile(
               "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
               " [%0, {%1, %2}], [%3];" ::"l"((uint64_t)gmap),
@@ -810,7 +845,7 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (lane == 0) mbar_arrive(tempty(acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (issuer) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncwarp();
   }
 
@@ -879,16 +914,47 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D fp32 tensor [outer][inner] with a 32 x 32 box, 128-byte swizzle (TMA reduce target).
+// A row-major bf16 matrix [rows][inner] viewed as [inner/64][rows][64]: one
+// box is nchunk 128-byte-swizzled panels of 64 rows x 64 columns, 8 KiB apart
+// in shared memory, the same layout as nchunk 2D boxes of 64 x 64.
+static bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t nchunk) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[3] = {64, rows, inner / 64};
+  cuuint64_t gstride[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, 64, nchunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D fp32 tensor [outer][inner] with a 32 x 128 box, 128-byte swizzle (TMA reduce target).
 static bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return false;
   cuuint64_t gdim[2] = {inner, outer};
   cuuint64_t gstride[1] = {inner * 4};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {32, 128};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim, gstride, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D fp32 tensor [outer][inner] with a box of 128 rows x box_inner, no swizzle
+// (L2 prefetch of a weight-gradient tile).
+static bool encode_2d_f32_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                               uint32_t box_inner) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -925,7 +991,8 @@ static int sm_count_gemm() {
 
 static int pick_bn(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
 
-// The two weight tensors as 2D [rows][H'] maps with a box of box_outer rows.
+// The two weight tensors as 2D [rows][H'] maps with a box of box_outer rows
+// (the input gradient reads them K-major).
 static bool encode_weights(const Dims& d, const void* w_home, const void* w_slot,
                            uint32_t box_outer, CUtensorMap* twh, CUtensorMap* tws) {
   if (!encode_2d(twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, box_outer)) return false;
@@ -940,8 +1007,13 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
                                 int* launches) {
   CUtensorMap ta, twh, tws;
   if (!encode_2d(&ta, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, kMmaM)) return cudaErrorInvalidValue;
-  if (!encode_weights(d, w_home, w_slot, 64, &twh, &tws)) return cudaErrorInvalidValue;
   const int bn = pick_bn(d.Hp);
+  const bool slots = (w_slot != nullptr && d.B > 0);
+  if (!encode_panels_3d(&twh, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, bn / 64))
+    return cudaErrorInvalidValue;
+  if (!encode_panels_3d(&tws, slots ? w_slot : w_home, (uint64_t)d.Hp,
+                        slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, bn / 64))
+    return cudaErrorInvalidValue;
   const long long max_tiles = (long long)d.max_mtiles * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_tiles));
   const GemmShape sh{d.H, d.Hp, d.H};
@@ -977,26 +1049,34 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void*
                                    const void* dy, float* g_home, float* g_slot, cudaStream_t st,
                                    int* launches) {
   CUtensorMap tx, tdy, tgh, tgs;
-  if (!encode_2d(&tx, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
-  if (!encode_2d(&tdy, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 64)) return cudaErrorInvalidValue;
+  if (!encode_panels_3d(&tx, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, 2)) return cudaErrorInvalidValue;
+  if (!encode_panels_3d(&tdy, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, (uint32_t)pick_bn(d.Hp) / 64))
+    return cudaErrorInvalidValue;
   if (!encode_2d_f32(&tgh, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H)) return cudaErrorInvalidValue;
   const bool slots = g_slot != nullptr && d.B > 0;
   if (!encode_2d_f32(&tgs, slots ? g_slot : g_home, (uint64_t)d.Hp,
                      slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H))
     return cudaErrorInvalidValue;
   const int bn = pick_bn(d.Hp);
+  // L2 prefetch views of G: one box is a whole 128 x BN work-item tile
+  CUtensorMap tghp, tgsp;
+  if (!encode_2d_f32_tile(&tghp, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, (uint32_t)bn))
+    return cudaErrorInvalidValue;
+  if (!encode_2d_f32_tile(&tgsp, slots ? g_slot : g_home, (uint64_t)d.Hp,
+                          slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, (uint32_t)bn))
+    return cudaErrorInvalidValue;
   const long long max_items = (long long)d.max_groups * (d.H / kMmaM) * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_items));
   cudaError_t e;
   if (bn == 256) {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, tgh, tgs, d, p);
+    e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, tgh, tgs, tghp, tgsp, d, p);
   } else if (bn == 128) {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<128, 5>>(k_ggemm_dw<128, 5>, set, grid, st, tx, tdy, tgh, tgs, d, p);
+    e = launch_cfg<GemmCfgDW<128, 5>>(k_ggemm_dw<128, 5>, set, grid, st, tx, tdy, tgh, tgs, tghp, tgsp, d, p);
   } else {
     static bool set = false;
-    e = launch_cfg<GemmCfgDW<64, 7>>(k_ggemm_dw<64, 7>, set, grid, st, tx, tdy, tgh, tgs, d, p);
+    e = launch_cfg<GemmCfgDW<64, 7>>(k_ggemm_dw<64, 7>, set, grid, st, tx, tdy, tgh, tgs, tghp, tgsp, d, p);
   }
   if (e == cudaSuccess) *launches += 1;
   return e;
