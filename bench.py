@@ -42,15 +42,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def _profile_workload():
     from perfectly_balanced_token_gb300 import synthetic as syn
     # the pages shape's H, H', K with fewer experts and tokens: a few GB on the
-    # device; C*R/E = 4096 rows per group, so the GEMM runs 256-row work tiles
+    # device; ~4k rows per group, so the plans pick 256-row work tiles
     return syn.Workload("profile-sized", R=8, E=16, B=2, K=8, S=1024, H=7168, Hp=2048)
 
 
 def _profile128_workload():
     from perfectly_balanced_token_gb300 import synthetic as syn
-    # as above with E=24: C*R/E = 2731 rows per group, so 128-row work tiles
-    # (the GEMM variant the pages shape uses)
-    return syn.Workload("profile-sized-128", R=8, E=24, B=3, K=8, S=1024, H=7168, Hp=2048)
+    # as above with E=64: ~0.9k rows per group, so the plans pick 128-row work
+    # tiles (the GEMM variant the pages shape uses)
+    return syn.Workload("profile-sized-128", R=8, E=64, B=8, K=8, S=1024, H=7168, Hp=2048)
 
 
 def _pages():
@@ -276,7 +276,8 @@ def run_ours(args):
             counters.append({"fills": c[0], "mtiles": c[1], "occupied_slots": c[2],
                              "reduced_experts": c[3], "max_redundant_per_rank": int(n_recv.max()),
                              "link_bytes_per_entry": c[4] * (payload + 4),
-                             "link_bytes_send_once": c[5] * payload + c[4] * 4})
+                             "link_bytes_send_once": c[5] * payload + c[4] * 4,
+                             "gemm_tile_rows": c[7]})
 
         # the timed loop only replays graphs, so host-side enqueue cost never
         # shows up between the per-segment events
@@ -393,7 +394,9 @@ def run_ours(args):
     gemm_ms = float(seg[:, 3].mean())
     flops = 2.0 * N * w.H * w.Hp
     achieved_tf = flops / (gemm_ms / 1e3) / 1e12
-    gemm_kernel = "k_ggemm_m256" if (w.S * w.K * w.R >= 4096 * w.E) else "k_ggemm_m128"
+    # the variant the plans chose (the other one is launched and returns at once)
+    rows_chosen = sorted({c["gemm_tile_rows"] for c in counters})
+    gemm_kernel = "+".join("k_ggemm_m256" if r == 256 else "k_ggemm_m128" for r in rows_chosen)
     traffic = measured_traffic(gemm_kernel) if args.workload == "pages" else None
     roofline = {"kernel": f"{gemm_kernel} (moonep_grouped_gemm)", "bound": "tensor",
                 "achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",

@@ -57,11 +57,17 @@ typedef struct moonep_dims {
                          the rank with the largest surplus, donor experts in
                          descending remaining copies (fewest distinct experts
                          per fill) */
+  int32_t gemm_rows; /* height of the grouped GEMMs' work tiles ("Kimi K3 模型结构（8）",
+                        rank 内部: the schedule's parameters are fixed from the load
+                        before the GEMM runs):
+                        0 = chosen on the device at every plan by an analytic
+                            cost model over the plan's actual group sizes,
+                        128 or 256 = fixed (other values: MOONEP_ERR_ARG) */
 } moonep_dims;
 
 enum moonep_status {
   MOONEP_OK = 0,
-  MOONEP_ERR_ARG = 1,      /* null pointer, non-positive dimension, bad mode or policy */
+  MOONEP_ERR_ARG = 1,      /* null pointer, non-positive dimension, bad mode, policy or gemm_rows */
   MOONEP_ERR_ALIGN = 2,    /* a pointer is not 16-byte aligned                 */
   MOONEP_ERR_SLOTS = 3,    /* training mode with B < E/R                       */
   MOONEP_ERR_SHAPE = 4,    /* E % R != 0, K > E, E > 4096, H or Hp not a multiple
@@ -114,7 +120,8 @@ enum moonep_counter {
   MOONEP_CNT_REDUCE = 3,   /* home experts with at least one slot copy     */
   MOONEP_CNT_REMOTE_ENTRIES = 4, /* route entries whose destination is not the token's own rank */
   MOONEP_CNT_REMOTE_PAIRS = 5,   /* distinct (token, destination rank) pairs among those       */
-  MOONEP_CNT_GROUPS = 6          /* non-empty (rank, weight row) groups                         */
+  MOONEP_CNT_GROUPS = 6,         /* non-empty (rank, weight row) groups                         */
+  MOONEP_CNT_TILE_ROWS = 7       /* work-tile height the plan chose for the GEMMs (128 or 256)  */
 };
 
 /* Size in bytes of the plan workspace for `dims` (host only, no CUDA call).

@@ -30,7 +30,8 @@ class MoonepError(RuntimeError):
 
 
 class moonep_dims(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("R", "E", "B", "K", "S", "H", "Hp", "mode", "policy")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("R", "E", "B", "K", "S", "H", "Hp", "mode", "policy",
+                                               "gemm_rows")]
 
     @property
     def L(self):
@@ -109,8 +110,9 @@ def status_string(status: int) -> str:
         return "library not loaded"
 
 
-def dims(R, E, B, K, S, H, Hp, mode=0, policy=0) -> moonep_dims:
-    return moonep_dims(R, E, B, K, S, H, Hp, mode, policy)
+def dims(R, E, B, K, S, H, Hp, mode=0, policy=0, gemm_rows=0) -> moonep_dims:
+    """gemm_rows: 0 lets each plan choose the GEMM work-tile height; 128 or 256 fixes it."""
+    return moonep_dims(R, E, B, K, S, H, Hp, mode, policy, gemm_rows)
 
 
 def _check(rc: int, what: str):

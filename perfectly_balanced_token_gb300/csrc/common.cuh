@@ -16,7 +16,6 @@ constexpr int kMmaM = 128;          // rows of one tcgen05.mma (cta_group::1)
 // tiles (two accumulators share each weight panel: fewer L2->SM bytes per
 // flop); smaller groups use 128-row tiles, which keep fewer groups' weights in
 // flight at once and so hit L2 more often.
-constexpr int kBigGroupRows = 4096;
 constexpr int kHistWarps = 8;
 
 // Per-expert migrated range of global ordinals [lo, hi) and where it goes.
@@ -24,7 +23,7 @@ struct Piece {
   int32_t lo, hi, u, g;
 };
 
-// One GEMM work tile of up to Dims::tile_m rows: recv/y row of its first row, valid rows, the weight
+// One GEMM work tile of up to 128 or 256 rows (the height the plan chose): recv/y row of its first row, valid rows, the weight
 // it multiplies (>= 0: home expert id; < 0: -1 - slot id u*B+j) and its rank.
 struct MTile {
   int32_t row0, rows, wsel, u;
@@ -65,7 +64,7 @@ struct Dims {
   int R, E, B, K, S, H, Hp, mode, policy;
   int L, C, N;
   int nchunk, chunk_tokens, max_mtiles, max_groups;
-  int tile_m;  // GEMM work-tile height: 128 or 256 rows
+  int tile_m;  // GEMM work-tile height fixed by the caller (128 or 256), or 0: chosen per plan
 };
 
 // Workspace layout (host computes it; kernels receive resolved pointers).

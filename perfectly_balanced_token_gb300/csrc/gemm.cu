@@ -7,8 +7,12 @@
 // multiplied by W_home[g] (g < E) or by slot (u, g-E).
 //
 // Design (sm_103a):
+//  * two variants, with work tiles of 128 rows (k_ggemm_m128) and of 256 rows
+//    (k_ggemm_m256); every plan picks one with the cost model of
+//    gemm_cost.cuh and records it in the workspace.  Both are launched; the
+//    one not chosen returns before touching anything.
 //  * persistent CTAs, one per SM; the work list is the planner's list of
-//    work tiles of up to 256 rows of one group (device memory), times H'/BN
+//    work tiles of up to 128 or 256 rows of one group (device memory), times H'/BN
 //    column tiles.  Column tiles of one row tile are adjacent in the order, so
 //    concurrently running CTAs share the A rows and all tiles of one group
 //    share the expert's weights in L2.
@@ -258,6 +262,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
+  if (p.counters[MOONEP_CNT_TILE_ROWS] != kMmaM) return;  // the plan chose 256-row tiles
   const int NT = sh.N / BN;
   const int total = p.counters[MOONEP_CNT_MTILES] * NT;
   const int KB = sh.K / kBK;
@@ -431,6 +436,7 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
+  if (p.counters[MOONEP_CNT_TILE_ROWS] != 2 * kMmaM) return;  // the plan chose 128-row tiles
   const int NT = sh.N / BN;
   const int total = p.counters[MOONEP_CNT_MTILES] * NT;
   const int KB = sh.K / kBK;
@@ -973,13 +979,25 @@ static cudaError_t launch_cfg(KernelT kernel, bool& attr_set, int grid, cudaStre
 template <int BN, int S128, int S256, bool BKM>
 static cudaError_t launch_bn(const Dims& d, GemmShape sh, const PlanPtrs& p, const CUtensorMap& a,
                              const CUtensorMap& wh, const CUtensorMap& ws, uint16_t* y, int grid,
-                             cudaStream_t st) {
+                             cudaStream_t st, int* launches) {
+  // With the height left to the plan both variants are launched; the one the
+  // plan did not choose returns at once (the choice is only on the device).
   static bool set128 = false, set256 = false;
-  if (d.tile_m == 256)
-    return launch_cfg<GemmCfgM256<BN, S256>>(k_ggemm_m256<BN, S256, BKM>, set256, grid, st, a, wh,
-                                             ws, d, sh, p, y);
-  return launch_cfg<GemmCfgM128<BN, S128>>(k_ggemm_m128<BN, S128, BKM>, set128, grid, st, a, wh, ws,
-                                           d, sh, p, y);
+  int n = 0;
+  if (d.tile_m != 2 * kMmaM) {
+    const cudaError_t e = launch_cfg<GemmCfgM128<BN, S128>>(k_ggemm_m128<BN, S128, BKM>, set128,
+                                                            grid, st, a, wh, ws, d, sh, p, y);
+    if (e != cudaSuccess) return e;
+    ++n;
+  }
+  if (d.tile_m != kMmaM) {
+    const cudaError_t e = launch_cfg<GemmCfgM256<BN, S256>>(k_ggemm_m256<BN, S256, BKM>, set256,
+                                                            grid, st, a, wh, ws, d, sh, p, y);
+    if (e != cudaSuccess) return e;
+    ++n;
+  }
+  *launches += n;
+  return cudaSuccess;
 }
 
 static int sm_count_gemm() {
@@ -1018,10 +1036,10 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_tiles));
   const GemmShape sh{d.H, d.Hp, d.H};
   cudaError_t e;
-  if (bn == 256) e = launch_bn<256, 4, 3, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else if (bn == 128) e = launch_bn<128, 6, 4, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  else e = launch_bn<64, 8, 5, false>(d, sh, p, ta, twh, tws, (uint16_t*)y, grid, st);
-  if (e == cudaSuccess) *launches += 1;
+  uint16_t* out = (uint16_t*)y;
+  if (bn == 256) e = launch_bn<256, 4, 3, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  else if (bn == 128) e = launch_bn<128, 6, 4, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  else e = launch_bn<64, 8, 5, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   return e;
 }
 
@@ -1037,10 +1055,10 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const PlanPtrs& p, const void*
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_tiles));
   const GemmShape sh{d.Hp, d.H, d.H};
   cudaError_t e;
-  if (bn == 256) e = launch_bn<256, 4, 3, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
-  else if (bn == 128) e = launch_bn<128, 6, 4, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
-  else e = launch_bn<64, 8, 5, true>(d, sh, p, ta, twh, tws, (uint16_t*)d_recv, grid, st);
-  if (e == cudaSuccess) *launches += 1;
+  uint16_t* out = (uint16_t*)d_recv;
+  if (bn == 256) e = launch_bn<256, 4, 3, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  else if (bn == 128) e = launch_bn<128, 6, 4, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  else e = launch_bn<64, 8, 5, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   return e;
 }
 

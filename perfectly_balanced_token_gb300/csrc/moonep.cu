@@ -38,6 +38,7 @@ static int check_dims(const moonep_dims* in, Dims* d) {
     return MOONEP_ERR_ARG;
   if (x.mode != 0 && x.mode != 1) return MOONEP_ERR_ARG;
   if (x.policy != 0 && x.policy != 1) return MOONEP_ERR_ARG;
+  if (x.gemm_rows != 0 && x.gemm_rows != kMmaM && x.gemm_rows != 2 * kMmaM) return MOONEP_ERR_ARG;
   if (x.E % x.R != 0 || x.K > x.E || x.E > kMaxExperts || x.B > x.E) return MOONEP_ERR_SHAPE;
   if (x.H % 64 != 0 || x.Hp % 64 != 0) return MOONEP_ERR_SHAPE;
   const int64_t N = (int64_t)x.R * x.S * x.K;
@@ -55,8 +56,9 @@ static int check_dims(const moonep_dims* in, Dims* d) {
   d->chunk_tokens = std::max(1, kChunkCopies / x.K);
   d->nchunk = (x.S + d->chunk_tokens - 1) / d->chunk_tokens;
   const int64_t groups = std::min<int64_t>((int64_t)x.E + x.B, d->C);
-  d->tile_m = ((int64_t)d->C * x.R >= (int64_t)kBigGroupRows * x.E) ? 2 * kMmaM : kMmaM;
-  const int64_t mt = (N + d->tile_m - 1) / d->tile_m + (int64_t)x.R * groups;
+  d->tile_m = x.gemm_rows;  // 0: the planner chooses per plan
+  // room for the longer (128-row) tile list whatever is chosen
+  const int64_t mt = (N + kMmaM - 1) / kMmaM + (int64_t)x.R * groups;
   if (mt >= (int64_t(1) << 31)) return MOONEP_ERR_SHAPE;
   d->max_mtiles = (int)mt;
   d->max_groups = (int)std::min<int64_t>((int64_t)x.R * groups, int64_t(1) << 30);
@@ -347,7 +349,7 @@ int moonep_plan_export(const moonep_dims* dims, const void* plan_ws, void* host_
 const char* moonep_status_string(int s) {
   switch (s) {
     case MOONEP_OK: return "ok";
-    case MOONEP_ERR_ARG: return "invalid argument (null pointer, non-positive dimension, bad mode or policy)";
+    case MOONEP_ERR_ARG: return "invalid argument (null pointer, non-positive dimension, bad mode, policy or gemm_rows)";
     case MOONEP_ERR_ALIGN: return "pointer not 16-byte aligned";
     case MOONEP_ERR_SLOTS: return "training mode needs B >= E/R prefetch slots";
     case MOONEP_ERR_SHAPE: return "unsupported shape (E%R, K>E, E>4096, B>E, H or Hp not a multiple of 64, or a size >= 2^31)";

@@ -14,6 +14,7 @@
 // section 在线规划、零拷贝、静态 shape: static shapes remove the per-layer host
 // synchronisation).
 #include "common.cuh"
+#include "gemm_cost.cuh"
 
 namespace moonep {
 
@@ -100,8 +101,10 @@ k_plan(Dims d, PlanPtrs p) {
   int32_t* sMig = sT + d.E;         // [E]
   int32_t* sLoad = sMig + d.E;      // [R]
   int32_t* sState = sLoad + d.R;    // [R]
-  int32_t* sTiles = sState + d.R;   // [R]
-  int32_t* sGroups = sTiles + d.R;  // [R] non-empty weight-row groups per rank
+  int32_t* sT128 = sState + d.R;    // [R] 128-row work tiles per rank
+  int32_t* sT256F = sT128 + d.R;    // [R] 256-row work tiles with more than 128 rows
+  int32_t* sT256H = sT256F + d.R;   // [R] 256-row work tiles with at most 128 rows
+  int32_t* sGroups = sT256H + d.R;  // [R] non-empty weight-row groups per rank
   int32_t* sPieceN = sGroups + d.R; // [E] pieces per expert so far
   if (plan_failed(p.status)) return;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -136,7 +139,9 @@ k_plan(Dims d, PlanPtrs p) {
   for (int h = tid; h < d.R; h += nt) {
     p.n_recv[h] = 0;
     p.src[h] = -1;
-    sTiles[h] = 0;
+    sT128[h] = 0;
+    sT256F[h] = 0;
+    sT256H[h] = 0;
     sGroups[h] = 0;
   }
   for (int i = tid; i < 3 * max(d.R - 1, 1); i += nt) p.fills[i] = -1;
@@ -149,6 +154,15 @@ k_plan(Dims d, PlanPtrs p) {
     sState[h] = s < d.C ? kUnder : (s > d.C ? kOver : kBalanced);
   }
   __syncthreads();
+
+  // a non-empty group of `rows` rows on rank u: its work tiles at both heights
+  auto count_group = [&](int u, int rows) {
+    atomicAdd(&sT128[u], (rows + kMmaM - 1) / kMmaM);
+    const int rem = rows % (2 * kMmaM);
+    atomicAdd(&sT256F[u], rows / (2 * kMmaM) + (rem > kMmaM ? 1 : 0));
+    if (rem > 0 && rem <= kMmaM) atomicAdd(&sT256H[u], 1);
+    atomicAdd(&sGroups[u], 1);
+  };
 
   // the fills, sequential by construction (at most R-1 of them); warp 0 runs
   // them, each decision made with ballots / shuffles so all lanes agree
@@ -167,8 +181,7 @@ k_plan(Dims d, PlanPtrs p) {
       p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
       sPieceN[e] = pi + 1;
       p.cu[(size_t)u * (EB + 1) + g + 1] = t;
-      atomicAdd(&sTiles[u], (t + d.tile_m - 1) / d.tile_m);
-      atomicAdd(&sGroups[u], 1);
+      count_group(u, t);
       sMig[e] += t;
       return true;
     };
@@ -280,8 +293,7 @@ k_plan(Dims d, PlanPtrs p) {
     p.keep[e] = k;
     const int h = e / d.L;
     p.cu[(size_t)h * (EB + 1) + e + 1] = k;
-    atomicAdd(&sTiles[h], (k + d.tile_m - 1) / d.tile_m);
-    if (k > 0) atomicAdd(&sGroups[h], 1);
+    if (k > 0) count_group(h, k);
   }
   // reduce lists: the slots holding e in ascending (u, j)
   for (int s = tid; s < d.R * d.B; s += nt) {
@@ -322,10 +334,21 @@ k_plan(Dims d, PlanPtrs p) {
     if (tid == 0) {
       p.counters[MOONEP_CNT_OCCUPIED] = n_occ;
       p.counters[MOONEP_CNT_REDUCE] = n_red;
+      // the GEMMs' work-tile height: fixed by the dims, or the cheaper one
+      // under the cost model for this plan's group sizes
+      long long n128 = 0, n256f = 0, n256h = 0, ng = 0;
+      for (int h = 0; h < d.R; ++h) {
+        n128 += sT128[h];
+        n256f += sT256F[h];
+        n256h += sT256H[h];
+        ng += sGroups[h];
+      }
+      const int rows = d.tile_m ? d.tile_m : gemm_tile_rows_for(n128, n256f, n256h, ng, d.Hp);
+      p.counters[MOONEP_CNT_TILE_ROWS] = rows;
       int run = 0;
       for (int h = 0; h < d.R; ++h) {
         p.rank_tiles[h] = run;
-        run += sTiles[h];
+        run += (rows == kMmaM) ? sT128[h] : sT256F[h] + sT256H[h];
       }
       p.rank_tiles[d.R] = run;
       p.counters[MOONEP_CNT_MTILES] = run;
@@ -385,13 +408,14 @@ k_tables(Dims d, PlanPtrs p) {
   // each thread scans a contiguous run of groups
   const int per = (EB + 1023) / 1024;
   const int g0 = min(EB, tid * per), g1 = min(EB, g0 + per);
+  const int tile_m = p.counters[MOONEP_CNT_TILE_ROWS];
   int rows_local[8];
   int rsum = 0, tsum = 0, gsum = 0;
   for (int g = g0, i = 0; g < g1; ++g, ++i) {
     const int rows = cu[g + 1];
     if (i < 8) rows_local[i] = rows;
     rsum += rows;
-    tsum += (rows + d.tile_m - 1) / d.tile_m;
+    tsum += (rows + tile_m - 1) / tile_m;
     gsum += rows > 0;
   }
   int ra = rsum, tb = tsum, gc = gsum;
@@ -402,8 +426,8 @@ k_tables(Dims d, PlanPtrs p) {
     const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 5 for E <= 4096
     cu[g] = row;
     const int wsel = (g < d.E) ? g : -1 - (u * d.B + (g - d.E));
-    for (int m = 0; m * d.tile_m < rows; ++m) {
-      p.mtiles[tile++] = MTile{u * d.C + row + m * d.tile_m, min(d.tile_m, rows - m * d.tile_m), wsel, u};
+    for (int m = 0; m * tile_m < rows; ++m) {
+      p.mtiles[tile++] = MTile{u * d.C + row + m * tile_m, min(tile_m, rows - m * tile_m), wsel, u};
     }
     if (rows > 0) p.groups[grp++] = MTile{u * d.C + row, rows, wsel, u};
     row += rows;
@@ -506,7 +530,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     if (err != cudaSuccess) return err;
   }
   k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
-  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 4 * d.R);
+  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 6 * d.R);
   if (plan_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;

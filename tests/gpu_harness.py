@@ -28,8 +28,8 @@ def odims(w, policy=0) -> oplanner.Dims:
                          policy=policy)
 
 
-def cdims(w, policy=0):
-    return mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy)
+def cdims(w, policy=0, gemm_rows=0):
+    return mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy, gemm_rows)
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, what: str):
@@ -74,8 +74,8 @@ def compare_plan(tabs: dict, fp: dict, d: oplanner.Dims):
 class Run:
     """Device buffers and one pass of the CUDA path for a workload."""
 
-    def __init__(self, w, routing, seed=0, guard=4096, policy=0):
-        self.w, self.d, self.od = w, cdims(w, policy), odims(w, policy)
+    def __init__(self, w, routing, seed=0, guard=4096, policy=0, gemm_rows=0):
+        self.w, self.d, self.od = w, cdims(w, policy, gemm_rows), odims(w, policy)
         self.routing = routing
         dev = "cuda"
         self.ws = mx.PlanWorkspace(self.d)

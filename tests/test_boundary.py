@@ -59,12 +59,18 @@ def test_dims_validation():
             mx.moonep_plan_workspace_bytes(d)
         assert ei.value.status == _lib.ERR_SHAPE
     for d in [mx.dims(0, 8, 2, 2, 16, 64, 64), mx.dims(4, 8, -1, 2, 16, 64, 64, 1),
-              mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 2)]:
+              mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 2), mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 0, 64),
+              mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 0, 512)]:
         with pytest.raises(mx.MoonepError) as ei:
             mx.moonep_plan_workspace_bytes(d)
         assert ei.value.status == _lib.ERR_ARG
     # inference mode accepts B < E/R, including B = 0
     assert mx.moonep_plan_workspace_bytes(mx.dims(8, 384, 0, 8, 8192, 7168, 2048, 1)) > 0
+    # the work-tile height may be left to the plan or fixed; the workspace has
+    # room for the longer tile list either way
+    sizes = {r: mx.moonep_plan_workspace_bytes(mx.dims(8, 384, 48, 8, 8192, 7168, 2048, 0, 0, r))
+             for r in (0, 128, 256)}
+    assert sizes[0] == sizes[128] == sizes[256] > 0
 
 
 def test_layout_tables_are_aligned_and_inside():

@@ -46,11 +46,11 @@ def _lib():
     gh.ensure_library()
 
 
-def _setup(w, mk, policy):
+def _setup(w, mk, policy, gemm_rows=0):
     rt = mk(w)
     od = gh.odims(w, policy)
     fp = oplanner.full_plan(rt.idx, od)
-    run = gh.Run(w, rt, policy=policy)
+    run = gh.Run(w, rt, policy=policy, gemm_rows=gemm_rows)
     run.plan()
     return rt, od, fp, run
 
@@ -74,6 +74,26 @@ def test_combine_backward(name, w, mk, policy):
 @pytest.mark.parametrize("name,w,mk,policy", CASES, ids=[c[0] for c in CASES])
 def test_grouped_gemm_dx(name, w, mk, policy):
     rt, od, fp, run = _setup(w, mk, policy)
+    mx.moonep_prefetch_weights(run.d, run.ws.buf, run.w_home, run.w_slot)
+    dy = syn.normal_bf16((w.N, w.Hp), 1.0, 83).cuda()
+    drecv = torch.zeros(w.N * w.H, dtype=torch.bfloat16, device="cuda")
+    mx.moonep_grouped_gemm_dx(run.d, run.ws.buf, dy.view(-1), run.w_home, run.w_slot, drecv)
+    dst = fp["dst"].reshape(-1)
+    per_e = olayer.expert_backward(gh.host_bits(run.x), gh.host_bits(run.w_home), rt.idx,
+                                   gh.host_bits(dy)[dst], od)
+    got = gh.bf16_to_np(drecv).reshape(w.N, w.H)
+    for e, (cids, want, _) in per_e.items():
+        if cids.size:
+            gh.assert_close(got[dst[cids]], olayer.bf16_to_f64(want), f"{name} dRecv expert {e}")
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("name,w,mk,policy", [CASES[0], CASES[5], CASES[6]],
+                         ids=[CASES[i][0] for i in (0, 5, 6)])
+def test_grouped_gemm_dx_fixed_tile_rows(name, w, mk, policy, rows):
+    """The input-gradient GEMM with the work-tile height fixed either way."""
+    rt, od, fp, run = _setup(w, mk, policy, gemm_rows=rows)
+    assert int(run.ws.tables()["counters"][7]) == rows
     mx.moonep_prefetch_weights(run.d, run.ws.buf, run.w_home, run.w_slot)
     dy = syn.normal_bf16((w.N, w.Hp), 1.0, 83).cuda()
     drecv = torch.zeros(w.N * w.H, dtype=torch.bfloat16, device="cuda")

@@ -68,10 +68,60 @@ CASES = [
 
 @pytest.mark.parametrize("name,w,mk", CASES, ids=[c[0] for c in CASES])
 def test_layer_parity(name, w, mk):
+    _layer_parity(name, w, mk(w), 0)
+
+
+# the GEMM work-tile height fixed either way (the plan and every output must
+# not depend on it)
+FIXED_ROWS_CASES = [c for c in CASES if c[0] in (
+    "r8e64-maxvio1", "r5-e20-ragged", "infer-b1-overflow", "m256-bn256", "m256-bn64-ragged",
+    "bn256-ragged")]
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("name,w,mk", FIXED_ROWS_CASES, ids=[c[0] for c in FIXED_ROWS_CASES])
+def test_layer_parity_fixed_tile_rows(name, w, mk, rows):
+    run = _layer_parity(name, w, mk(w), rows)
+    assert int(run.ws.tables()["counters"][7]) == rows
+
+
+def _cost_model():
+    """Coefficients of the GEMM tile-height cost model, read from its header."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(mx.__file__), "csrc", "gemm_cost.cuh")).read()
+    return {k: float(v) for k, v in re.findall(r"constexpr float (kCost\w+) = ([-0-9.e+]+)f;", src)}
+
+
+@pytest.mark.parametrize("name,w,mk", CASES, ids=[c[0] for c in CASES])
+def test_tile_rows_follow_the_cost_model(name, w, mk):
+    """With the height left to the plan, the planner's choice equals the cost
+    model evaluated on the plan's own group sizes (from cu_seqlens)."""
     rt = mk(w)
+    run = gh.Run(w, rt)
+    tabs = run.plan()
+    rows = np.diff(tabs["cu_seqlens"].astype(np.int64), axis=1).reshape(-1)
+    rows = rows[rows > 0]
+    rem = rows % 256
+    n128 = np.sum((rows + 127) // 128)
+    n256f = np.sum(rows // 256 + (rem > 128))
+    n256h = np.sum((rem > 0) & (rem <= 128))
+    c = _cost_model()
+    waves = float(n128) * (w.Hp / 256.0) / 152.0
+    t128 = c["kCostA128"] * n128 + c["kCostG128"] * rows.size + c["kCostW128"] * n128 * waves
+    t256 = (c["kCostA256Full"] * n256f + c["kCostA256Half"] * n256h + c["kCostG256"] * rows.size
+            + c["kCostW256"] * n256f * waves)
+    want = 256 if t256 < t128 else 128
+    if abs(float(t256) - float(t128)) <= 1e-4 * float(t128):  # a tie up to rounding: either
+        want = int(tabs["counters"][7])
+    assert int(tabs["counters"][7]) == want
+    assert int(tabs["counters"][1]) == (n128 if want == 128 else n256f + n256h)
+
+
+def _layer_parity(name, w, rt, gemm_rows):
     od = gh.odims(w)
     fp = oplanner.full_plan(rt.idx, od)
-    run = gh.Run(w, rt)
+    run = gh.Run(w, rt, gemm_rows=gemm_rows)
     run.forward()
 
     # plan: bit-exact, and Theorem 1 invariants on the GPU's own tables
@@ -107,6 +157,7 @@ def test_layer_parity(name, w, mk):
     gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(out_want),
                     f"{name} combine")
     run.check_all_guards()
+    return run
 
 
 @pytest.mark.parametrize("name,w,mk", CASES[:6], ids=[c[0] for c in CASES[:6]])
