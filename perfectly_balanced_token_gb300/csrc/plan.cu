@@ -10,7 +10,7 @@
 // descending id; inside an expert the highest global ordinals first.
 //
 // Everything stays on the device: the histogram, plan and tables are produced
-// by four launches whose shapes depend only on the dims ("Kimi K3 模型结构（8）",
+// by six launches whose shapes depend only on the dims ("Kimi K3 模型结构（8）",
 // section 在线规划、零拷贝、静态 shape: static shapes remove the per-layer host
 // synchronisation).
 #include "common.cuh"
@@ -90,7 +90,63 @@ k_hist(Dims d, const int32_t* __restrict__ idx, PlanPtrs p) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. single-CTA planner: chunk bases, loads, the fills, slots and row counts
+// 1b. chunk bases: for every expert, the exclusive prefix of its per-chunk
+//     counts in ascending (rank, chunk) order -- ascending (rank, token), the
+//     order of the global ordinals -- and its total T_e.  One CTA per 32
+//     experts: lane = expert, so every load is one coalesced row of 32 counts;
+//     warp w takes a contiguous run of the (rank, chunk) rows and the 32 runs
+//     are chained by a scan in shared memory.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+k_scan(Dims d, PlanPtrs p) {
+  __shared__ int32_t part[32][33];
+  if (plan_failed(p.status)) return;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int rc = d.R * d.nchunk;
+  const int per = (rc + 31) / 32;
+  const int i0 = min(rc, w * per), i1 = min(rc, i0 + per);
+  int32_t* c = p.counts + e;
+  constexpr int kBatch = 8;  // loads in flight before the dependent sum / stores
+  int sum = 0;
+  if (e < d.E) {
+    for (int b = i0; b < i1; b += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = (b + j < i1) ? c[(size_t)(b + j) * d.E] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) sum += v[j];
+    }
+  }
+  part[w][lane] = sum;
+  __syncthreads();
+  if (w == 0) {
+    int run = 0;
+    for (int k = 0; k < 32; ++k) {
+      const int v = part[k][lane];
+      part[k][lane] = run;
+      run += v;
+    }
+    if (e < d.E) p.T[e] = run;
+  }
+  __syncthreads();
+  if (e < d.E) {
+    int run = part[w][lane];
+    for (int b = i0; b < i1; b += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = (b + j < i1) ? c[(size_t)(b + j) * d.E] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (b + j < i1) c[(size_t)(b + j) * d.E] = run;
+        run += v[j];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. single-CTA planner: loads, the fills, slots and row counts
 // ---------------------------------------------------------------------------
 enum : int32_t { kBalanced = 0, kUnder = 1, kOver = 2 };
 
@@ -110,26 +166,9 @@ k_plan(Dims d, PlanPtrs p) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int EB = d.E + d.B;
 
-  // chunk bases (ascending (rank, chunk) == ascending (rank, token)) and T
-  const int rc = d.R * d.nchunk;
+  // T from the chunk scan
   for (int e = tid; e < d.E; e += nt) {
-    int run = 0;
-    int32_t* c = p.counts + e;
-    // 16 loads in flight before their stores: a load after a store to the same
-    // array would otherwise wait for the previous one
-    constexpr int kBatch = 16;
-    for (int i0 = 0; i0 < rc; i0 += kBatch) {
-      int v[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) v[j] = (i0 + j < rc) ? c[(size_t)(i0 + j) * d.E] : 0;
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        if (i0 + j < rc) c[(size_t)(i0 + j) * d.E] = run;
-        run += v[j];
-      }
-    }
-    sT[e] = run;
-    p.T[e] = run;
+    sT[e] = p.T[e];
     sMig[e] = 0;
     sPieceN[e] = 0;
     p.red_n[e] = 0;
@@ -535,11 +574,12 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;
   }
+  k_scan<<<(d.E + 31) / 32, 1024, 0, st>>>(d, p);
   k_plan<<<1, 1024, plan_smem, st>>>(d, p);
   k_tables<<<d.R, 1024, 0, st>>>(d, p);
   k_dst<<<dim3(d.nchunk, d.R), 256, 0, st>>>(d, idx, p);
   k_route<<<(d.R * d.S + 255) / 256, 256, 0, st>>>(d, p);
-  *launches += 5;
+  *launches += 6;
   return cudaGetLastError();
 }
 
