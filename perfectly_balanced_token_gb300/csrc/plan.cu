@@ -485,18 +485,22 @@ k_tables(Dims d, PlanPtrs p) {
 }
 
 // ---------------------------------------------------------------------------
-// 4. destinations and inverse: grid (nchunk, R), 256 threads
+// 4. destinations and inverse: grid (nchunk * kDstSplit, R), 256 threads;
+//    the kDstSplit CTAs of a chunk interleave its copies, so each thread
+//    follows at most four copies' chains of dependent loads
 // ---------------------------------------------------------------------------
+constexpr int kDstSplit = 4;
+
 __global__ void __launch_bounds__(256)
 k_dst(Dims d, const int32_t* __restrict__ idx, PlanPtrs p) {
   if (plan_failed(p.status)) return;
-  const int r = blockIdx.y, chunk = blockIdx.x;
+  const int r = blockIdx.y, chunk = blockIdx.x / kDstSplit, part = blockIdx.x % kDstSplit;
   const int t0 = chunk * d.chunk_tokens;
   const int t1 = min(d.S, t0 + d.chunk_tokens);
   const int ncopy = (t1 - t0) * d.K;
   const size_t first = ((size_t)r * d.S + t0) * d.K;
   const int32_t* base = p.counts + ((size_t)r * d.nchunk + chunk) * d.E;
-  for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
+  for (int i = part * blockDim.x + threadIdx.x; i < ncopy; i += kDstSplit * blockDim.x) {
     const size_t c = first + i;
     const int e = idx[c];
     const int q = base[e] + p.gidx[c];
@@ -535,11 +539,26 @@ k_route(Dims d, PlanPtrs p) {
     const int r = t / d.S;
     const int32_t* dt = p.dst + (size_t)t * d.K;
     int32_t* rt = p.route + (size_t)t * d.K;
+    // destination ranks of the first kRouteRegs entries kept in registers, so
+    // the earlier-entry test costs no reloads or divisions
+    constexpr int kRouteRegs = 32;
+    int ur[kRouteRegs];
+#pragma unroll
+    for (int j = 0; j < kRouteRegs; ++j) ur[j] = -1;
     for (int k = 0; k < d.K; ++k) {
       const int v = dt[k];
       const int u = v / d.C;
       bool dup = false;
-      for (int j = 0; j < k; ++j) dup |= (dt[j] / d.C == u);
+      if (k <= kRouteRegs) {
+#pragma unroll
+        for (int j = 0; j < kRouteRegs; ++j) dup |= (j < k) && (ur[j] == u);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kRouteRegs; ++j) dup |= (ur[j] == u);
+        for (int j = kRouteRegs; j < k; ++j) dup |= (dt[j] / d.C == u);
+      }
+#pragma unroll
+      for (int j = 0; j < kRouteRegs; ++j) ur[j] = (j == k) ? u : ur[j];
       const int off = v - u * d.C;
       rt[k] = dup ? -off - 1 : off;
       if (u != r) {
@@ -577,7 +596,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
   k_scan<<<(d.E + 31) / 32, 1024, 0, st>>>(d, p);
   k_plan<<<1, 1024, plan_smem, st>>>(d, p);
   k_tables<<<d.R, 1024, 0, st>>>(d, p);
-  k_dst<<<dim3(d.nchunk, d.R), 256, 0, st>>>(d, idx, p);
+  k_dst<<<dim3(d.nchunk * kDstSplit, d.R), 256, 0, st>>>(d, idx, p);
   k_route<<<(d.R * d.S + 255) / 256, 256, 0, st>>>(d, p);
   *launches += 6;
   return cudaGetLastError();
