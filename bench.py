@@ -396,7 +396,9 @@ def run_ours(args):
     achieved_tf = flops / (gemm_ms / 1e3) / 1e12
     # the variant the plans chose (the other one is launched and returns at once)
     rows_chosen = sorted({c["gemm_tile_rows"] for c in counters})
-    gemm_kernel = "+".join("k_ggemm_m256" if r == 256 else "k_ggemm_m128" for r in rows_chosen)
+    wide = w.Hp % 256 == 0  # 256-wide column tiles: 256-row tiles run on CTA pairs
+    gemm_kernel = "+".join(("k_ggemm_2sm" if wide else "k_ggemm_m256") if r == 256 else "k_ggemm_m128"
+                           for r in rows_chosen)
     traffic = measured_traffic(gemm_kernel) if args.workload == "pages" else None
     roofline = {"kernel": f"{gemm_kernel} (moonep_grouped_gemm)", "bound": "tensor",
                 "achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",

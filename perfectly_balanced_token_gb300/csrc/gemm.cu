@@ -606,6 +606,295 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   }
 }
 
+// ---- pair (cta_group::2) PTX ----------------------------------------------
+__device__ __forceinline__ uint32_t pair_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// the shared::cluster address of this CTA's shared-memory word `a` in CTA `rank`
+__device__ __forceinline__ uint32_t pair_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// TMA load into this CTA's shared memory, completing bytes on an mbarrier that
+// may sit in either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive once on the mbarrier at this offset in both CTAs of the pair when the
+// MMAs issued so far by this thread have completed
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_self(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+template <int STAGES>
+struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns of B
+  static constexpr int kABytes = kMmaM * kBK * 2;
+  static constexpr int kBBytes = 128 * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 512;  // two 128-lane x 256-column fp32 accumulators
+  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  // 32 KiB of slack past the barriers: one CTA per SM either way, and no
+  // operand read of the last stage can leave this CTA's allocation
+  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes + 32768;
+};
+
+// 256 x 256 work tiles on a CTA pair with the pair form of the MMA
+// (tcgen05 cta_group::2, M = 256): CTA c of a two-CTA cluster holds rows
+// 128c..128c+127 of the tile's A and columns 128c..128c+127 of its B panel;
+// one MMA instruction computes the whole 256 x 256 x 16 product, each SM's
+// tensor core producing its 128 rows from its own A and both halves of B.
+// Per K block each SM so loads 32 KiB for 128 x 256 x 64 of MMA work, where
+// the single-CTA 128-row kernel loads 48 KiB for the same work, and the
+// smaller stage buys six stages instead of four.
+// CTA 0 (the leader) issues the MMAs and owns the full, tempty and drain
+// barriers; both CTAs' loads complete on the leader's full barrier; each MMA
+// commit arrives on the empty (or tfull) barrier of both CTAs; each CTA drains
+// its own 128 accumulator rows and releases them on the leader's tempty.
+// Items are the 256-row tiles of the plan times H'/256 column tiles; a tile of
+// at most 128 rows leaves the second CTA's rows unused.
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
+            const __grid_constant__ CUtensorMap tm_ws, Dims d, GemmShape sh, PlanPtrs p,
+            uint16_t* __restrict__ y) {
+  using Cfg = GemmCfgPair<STAGES>;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  constexpr uint64_t kDrainNs = 200000000ull;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = pair_rank();
+  const bool leader = crank == 0;
+  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  if (plan_failed(p.status)) return;  // uniform over the pair: before any barrier
+  if (p.counters[MOONEP_CNT_TILE_ROWS] != 2 * kMmaM) return;
+  const int NT = sh.N / BN;
+  const int total = p.counters[MOONEP_CNT_MTILES] * NT;
+  const int KB = sh.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_wh);
+    prefetch_tmap(&tm_ws);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pair_sync();  // the peer's barriers are initialised before anything reaches them
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cl; t < total && ok; t += ncl) {
+        const MTile mt = p.mtiles[t / NT];
+        const int n0 = (t % NT) * BN + (int)crank * 128;
+        const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
+        const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * sh.wrows;
+        const int row0 = mt.row0 + (int)crank * kMmaM;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t fb = pair_map(full(stage), 0);
+          if (leader) mbar_expect_tx(full(stage), 2 * Cfg::kStageBytes);
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          tma_load_2d_pair(sa, &tm_a, fb, kb * kBK, row0);
+          tma_load_3d_pair(sa + Cfg::kABytes, wmap, fb, 0, wrow + kb * kBK, n0 / 64);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (ok) {
+        for (int i = 0; i < STAGES; ++i) {  // every fill released: no commit still in flight
+          if (!mbar_wait(empty(stage), phase ^ 1u, nullptr)) { ok = false; break; }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) set_error(p.status, MOONEP_ERR_TIMEOUT);
+      } else {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        if (leader) {
+          for (int i = 0; i < min(issued, STAGES); ++i) {
+            if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+            mbar_wait(full(stage), phase, nullptr, kDrainNs);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader only) ----------------
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = make_idesc(2 * kMmaM, BN, false, true);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = cl; t < total && ok; t += ncl) {
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
+            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            umma_bf16_pair(dtm, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit_pair_both(empty(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair_both(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        umma_commit_pair_self(drain);
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+    const int qw = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cl; t < total; t += ncl) {
+      const MTile mt = p.mtiles[t / NT];
+      const int n0 = (t % NT) * BN;
+      const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int row = (int)crank * kMmaM + qw * 32 + lane;
+      const bool valid = row < mt.rows;
+      uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
+      const uint32_t tbase = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tbase + c * 32, r);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+            o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+            o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+            o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(pair_map(tempty(acc), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  pair_sync();  // both CTAs done with TMEM and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+}
+
 // Weight gradient of the grouped GEMM: for every non-empty (rank u, weight
 // row g) group with rows a0..a1 of the receive buffer,
 //   G(u,g) += X[a0:a1]^T . dY[a0:a1]        ([H x H'], fp32),
@@ -1009,6 +1298,31 @@ static int sm_count_gemm() {
 
 static int pick_bn(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
 
+static bool set_fwd128 = false;
+
+// The CTA-pair kernel on two CTAs per co-resident cluster.
+static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs& p,
+                                    const CUtensorMap& a, const CUtensorMap& wh,
+                                    const CUtensorMap& ws, uint16_t* y, cudaStream_t st) {
+  using Cfg = GemmCfgPair<6>;
+  static int grid = 0;
+  if (grid == 0) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k_ggemm_2sm<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * std::max(1, sm_count_gemm() / 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, (void*)k_ggemm_2sm<6>, &cfg);
+    if (e != cudaSuccess) return e;
+    grid = 2 * std::max(1, ncl);
+  }
+  k_ggemm_2sm<6><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, sh, p, y);
+  return cudaGetLastError();
+}
+
 // The two weight tensors as 2D [rows][H'] maps with a box of box_outer rows
 // (the input gradient reads them K-major).
 static bool encode_weights(const Dims& d, const void* w_home, const void* w_slot,
@@ -1037,7 +1351,27 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
   const GemmShape sh{d.H, d.Hp, d.H};
   cudaError_t e;
   uint16_t* out = (uint16_t*)y;
-  if (bn == 256) e = launch_bn<256, 4, 3, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  if (bn == 256) {
+    // 128-row tiles: the single-CTA kernel; 256-row tiles: the CTA-pair kernel
+    if (d.tile_m != 2 * kMmaM) {
+      e = launch_cfg<GemmCfgM128<256, 4>>(k_ggemm_m128<256, 4, false>, set_fwd128, grid, st, ta, twh,
+                                          tws, d, sh, p, out);
+      if (e != cudaSuccess) return e;
+      *launches += 1;
+    }
+    if (d.tile_m != kMmaM) {
+      CUtensorMap twh2, tws2;  // B halves: 2 panels of 64 columns per CTA
+      if (!encode_panels_3d(&twh2, w_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 2))
+        return cudaErrorInvalidValue;
+      if (!encode_panels_3d(&tws2, slots ? w_slot : w_home, (uint64_t)d.Hp,
+                            slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, 2))
+        return cudaErrorInvalidValue;
+      e = launch_pair_gemm(d, sh, p, ta, twh2, tws2, out, st);
+      if (e != cudaSuccess) return e;
+      *launches += 1;
+    }
+    return cudaSuccess;
+  }
   else if (bn == 128) e = launch_bn<128, 6, 4, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   else e = launch_bn<64, 8, 5, false>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   return e;

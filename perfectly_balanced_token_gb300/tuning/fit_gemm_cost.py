@@ -153,9 +153,12 @@ def fit():
     for name, rpg, a, pa, b, pb, best, pick in rows:
         print(f"{name:16s} {rpg:8.0f} {a:8.3f} {pa:8.3f} {b:8.3f} {pb:8.3f}  {best} {pick}")
     right = sum(best == pick for *_, best, pick in rows)
+    picked = sum(a if pick == 128 else b for _, _, a, _, b, _, _, pick in rows)
+    fastest = sum(min(a, b) for _, _, a, _, b, _, _, _ in rows)
     err = max(max(abs(pa / a - 1), abs(pb / b - 1)) for _, _, a, pa, b, pb, _, _ in rows)
     print(f"choice matches the faster kernel on {right} of {len(rows)} workloads; "
-          f"largest relative error of a predicted time {err:.3f}")
+          f"largest relative error of a predicted time {err:.3f}; picked kernels' total time "
+          f"{picked / fastest - 1:+.2%} over the faster ones")
     src = open(HEADER).read()
     import re
     for name, val in coeffs.items():
