@@ -706,7 +706,7 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
 // its own 128 accumulator rows and releases them on the leader's tempty.
 // Items are the 256-row tiles of the plan times H'/256 column tiles; a tile of
 // at most 128 rows leaves the second CTA's rows unused.
-template <int STAGES>
+template <int STAGES, bool BKM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
             const __grid_constant__ CUtensorMap tm_ws, Dims d, GemmShape sh, PlanPtrs p,
@@ -782,7 +782,10 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
           if (leader) mbar_expect_tx(full(stage), 2 * Cfg::kStageBytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
           tma_load_2d_pair(sa, &tm_a, fb, kb * kBK, row0);
-          tma_load_3d_pair(sa + Cfg::kABytes, wmap, fb, 0, wrow + kb * kBK, n0 / 64);
+          if (BKM)  // 128 weight rows (this CTA's n), 64 k each
+            tma_load_2d_pair(sa + Cfg::kABytes, wmap, fb, kb * kBK, wrow + n0);
+          else      // two 64-column panels of 64 k-rows
+            tma_load_3d_pair(sa + Cfg::kABytes, wmap, fb, 0, wrow + kb * kBK, n0 / 64);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -807,7 +810,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   } else if (warp == 1) {
     // ---------------- MMA issuer (leader only) ----------------
     if (leader && lane == 0) {
-      constexpr uint32_t idesc = make_idesc(2 * kMmaM, BN, false, true);
+      constexpr uint32_t idesc = make_idesc(2 * kMmaM, BN, false, !BKM);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -823,7 +826,8 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 2), 16, 1024);
-            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            const uint64_t bd = BKM ? sw128_desc(sb + k * (kUmmaK * 2), 16, 1024)
+                                    : sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
             umma_bf16_pair(dtm, ad, bd, idesc, (kb | k) != 0);
           }
           umma_commit_pair_both(empty(stage));
@@ -1298,28 +1302,29 @@ static int sm_count_gemm() {
 
 static int pick_bn(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
 
-static bool set_fwd128 = false;
+static bool set_fwd128 = false, set_dx128 = false;
 
 // The CTA-pair kernel on two CTAs per co-resident cluster.
+template <bool BKM>
 static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs& p,
                                     const CUtensorMap& a, const CUtensorMap& wh,
                                     const CUtensorMap& ws, uint16_t* y, cudaStream_t st) {
   using Cfg = GemmCfgPair<6>;
   static int grid = 0;
   if (grid == 0) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_ggemm_2sm<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_ggemm_2sm<6, BKM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * std::max(1, sm_count_gemm() / 2));
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     int ncl = 0;
-    e = cudaOccupancyMaxActiveClusters(&ncl, (void*)k_ggemm_2sm<6>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&ncl, (void*)k_ggemm_2sm<6, BKM>, &cfg);
     if (e != cudaSuccess) return e;
     grid = 2 * std::max(1, ncl);
   }
-  k_ggemm_2sm<6><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, sh, p, y);
+  k_ggemm_2sm<6, BKM><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, sh, p, y);
   return cudaGetLastError();
 }
 
@@ -1366,7 +1371,7 @@ cudaError_t launch_grouped_gemm(const Dims& d, const PlanPtrs& p, const void* re
       if (!encode_panels_3d(&tws2, slots ? w_slot : w_home, (uint64_t)d.Hp,
                             slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, 2))
         return cudaErrorInvalidValue;
-      e = launch_pair_gemm(d, sh, p, ta, twh2, tws2, out, st);
+      e = launch_pair_gemm<false>(d, sh, p, ta, twh2, tws2, out, st);
       if (e != cudaSuccess) return e;
       *launches += 1;
     }
@@ -1390,7 +1395,23 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const PlanPtrs& p, const void*
   const GemmShape sh{d.Hp, d.H, d.H};
   cudaError_t e;
   uint16_t* out = (uint16_t*)d_recv;
-  if (bn == 256) e = launch_bn<256, 4, 3, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
+  if (bn == 256) {
+    // 128-row tiles: the single-CTA kernel; 256-row tiles: the CTA-pair kernel
+    if (d.tile_m != 2 * kMmaM) {
+      e = launch_cfg<GemmCfgM128<256, 4>>(k_ggemm_m128<256, 4, true>, set_dx128, grid, st, ta, twh,
+                                          tws, d, sh, p, out);
+      if (e != cudaSuccess) return e;
+      *launches += 1;
+    }
+    if (d.tile_m != kMmaM) {
+      CUtensorMap twh2, tws2;  // B halves: 128 weight rows (n) per CTA
+      if (!encode_weights(d, w_home, w_slot, 128, &twh2, &tws2)) return cudaErrorInvalidValue;
+      e = launch_pair_gemm<true>(d, sh, p, ta, twh2, tws2, out, st);
+      if (e != cudaSuccess) return e;
+      *launches += 1;
+    }
+    return cudaSuccess;
+  }
   else if (bn == 128) e = launch_bn<128, 6, 4, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   else e = launch_bn<64, 8, 5, true>(d, sh, p, ta, twh, tws, out, grid, st, launches);
   return e;

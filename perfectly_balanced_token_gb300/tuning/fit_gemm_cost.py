@@ -6,7 +6,8 @@
 `measure` plans a set of synthetic workloads whose rows per (rank, weight row)
 group range from a few hundred to several thousand, times the forward grouped
 GEMM with the work-tile height fixed at 128 and at 256 rows (CUDA events,
-L2 flushed between launches, median of several launches), and stores the
+L2 flushed between launches, the two heights launched alternately so that
+both see the same clock and power state, median of several launches), and stores the
 times with the tile and group counts of each plan in gemm_cost_measurements.json.
 
 `fit` fits, per tile height, non-negative coefficients of the model documented
@@ -31,6 +32,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "csrc", "gemm_cost.cuh")
 WORKLOADS = [
     ("pages-mv1", 8, 384, 48, 8, 8192, 7168, 2048, 1.0),
     ("pages-mv20", 8, 384, 48, 8, 8192, 7168, 2048, 20.0),
+    ("e384-s512", 8, 384, 48, 8, 512, 7168, 2048, 1.0),
+    ("e384-s1024", 8, 384, 48, 8, 1024, 7168, 2048, 1.0),
     ("e256", 8, 256, 32, 8, 1024, 7168, 2048, 1.0),
     ("e128", 8, 128, 16, 8, 1024, 7168, 2048, 1.0),
     ("e64", 8, 64, 8, 8, 1024, 7168, 2048, 1.0),
@@ -42,6 +45,7 @@ WORKLOADS = [
     ("e8-k4-s4096", 8, 8, 1, 4, 4096, 7168, 2048, 1.0),
     ("k3-mv1", 64, 896, 14, 16, 1024, 4096, 1024, 1.0),
     ("k3-mv10", 64, 896, 14, 16, 1024, 4096, 1024, 10.0),
+    ("h4096-e256", 8, 256, 32, 8, 1024, 4096, 1024, 1.0),
     ("h4096-e64", 8, 64, 8, 8, 2048, 4096, 1024, 1.0),
     ("h4096-e32", 8, 32, 4, 8, 2048, 4096, 1024, 1.0),
     ("h4096-e16", 8, 16, 2, 8, 2048, 4096, 1024, 1.0),
@@ -59,7 +63,7 @@ def tile_counts(cu: np.ndarray):
     return n128, n256f, n256h, int(rows.size)
 
 
-def measure(reps: int = 9):
+def measure(reps: int = 10):
     import torch
 
     sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
@@ -79,31 +83,36 @@ def measure(reps: int = 9):
         y = torch.empty(w.N * Hp, dtype=torch.bfloat16, device="cuda")
         rec = {"name": name, "R": R, "E": E, "B": B, "K": K, "S": S, "H": H, "Hp": Hp,
                "maxvio": float(syn.input_skew(rt.idx, E))}
+        # both heights planned up front, then launched alternately (ABBA...),
+        # so that neither sees a warmer or more power-capped GPU than the other
+        runs = {}
         for rows in (128, 256):
             d = mx.dims(R, E, B, K, S, H, Hp, 0, 0, rows)
             ws = mx.PlanWorkspace(d)
             mx.moonep_plan(d, idx, ws.buf)
             mx.moonep_prefetch_weights(d, ws.buf, wh, wsl)
             mx.moonep_dispatch(d, ws.buf, x, recv)
-            for _ in range(2):
-                mx.moonep_grouped_gemm(d, ws.buf, recv, wh, wsl, y)
-            torch.cuda.synchronize()
-            ts = []
-            for i in range(reps):
+            runs[rows] = (d, ws)
+        ts = {128: [], 256: []}
+        for i in range(reps + 2):
+            for rows in ((128, 256) if i % 2 == 0 else (256, 128)):
+                d, ws = runs[rows]
                 flush.fill_(i)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 mx.moonep_grouped_gemm(d, ws.buf, recv, wh, wsl, y)
                 b.record()
                 torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
+                if i >= 2:
+                    ts[rows].append(a.elapsed_time(b))
+        for rows in (128, 256):
+            d, ws = runs[rows]
             if mx.moonep_read_status(d, ws.buf) != 0:
                 raise RuntimeError(f"{name}: status {mx.moonep_read_status(d, ws.buf)}")
-            rec[f"ms{rows}"] = float(np.median(ts))
-            if rows == 128:
-                cu = ws.tables()["cu_seqlens"]
-                rec["n128"], rec["n256f"], rec["n256h"], rec["groups"] = tile_counts(cu)
-            del ws
+            rec[f"ms{rows}"] = float(np.median(ts[rows]))
+        cu = runs[128][1].tables()["cu_seqlens"]
+        rec["n128"], rec["n256f"], rec["n256h"], rec["groups"] = tile_counts(cu)
+        del runs
         print(json.dumps(rec), flush=True)
         out.append(rec)
         del x, wh, wsl, recv, y, idx
