@@ -6,8 +6,8 @@
 `measure` plans a set of synthetic workloads whose rows per (rank, weight row)
 group range from a few hundred to several thousand, times the forward grouped
 GEMM with the work-tile height fixed at 128 and at 256 rows (CUDA events,
-L2 flushed between launches, the two heights launched alternately so that
-both see the same clock and power state, median of several launches), and stores the
+L2 flushed and a 30 ms idle gap before every launch, the two heights launched
+alternately, median of several launches), and stores the
 times with the tile and group counts of each plan in gemm_cost_measurements.json.
 
 `fit` fits, per tile height, non-negative coefficients of the model documented
@@ -21,6 +21,7 @@ from __future__ import annotations
 import json
 import os
 import sys
+import time
 
 import numpy as np
 
@@ -98,6 +99,11 @@ def measure(reps: int = 10):
             for rows in ((128, 256) if i % 2 == 0 else (256, 128)):
                 d, ws = runs[rows]
                 flush.fill_(i)
+                # a short idle gap: every timed launch starts from the same
+                # settled clock and power state instead of inheriting the
+                # previous launch's
+                torch.cuda.synchronize()
+                time.sleep(0.03)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 mx.moonep_grouped_gemm(d, ws.buf, recv, wh, wsl, y)
@@ -171,7 +177,7 @@ def fit():
     src = open(HEADER).read()
     import re
     for name, val in coeffs.items():
-        src = re.sub(rf"constexpr float {name} = [^;]*;", f"constexpr float {name} = {val:.6g}f;", src)
+        src = re.sub(rf"constexpr float {name} = [^;]*;", f"constexpr float {name} = {val:.6e}f;", src)
     open(HEADER, "w").write(src)
 
 
