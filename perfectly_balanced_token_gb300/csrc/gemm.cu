@@ -709,8 +709,11 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
 // barriers; both CTAs' loads complete on the leader's full barrier; each MMA
 // commit arrives on the empty (or tfull) barrier of both CTAs; each CTA drains
 // its own 128 accumulator rows and releases them on the leader's tempty.
-// Items are the 256-row tiles of the plan times H'/256 column tiles; a tile of
-// at most 128 rows leaves the second CTA's rows unused.
+// Items are the 256-row tiles of the plan times N/256 column tiles; a tile of
+// at most 128 rows leaves the second CTA's rows unused.  BKM = false: the
+// forward product (B = W, N-major, two 64-column panels per CTA from one 3D
+// box); BKM = true: the input gradient (B = W^T, i.e. W read K-major, 128
+// weight rows per CTA).
 template <int STAGES, bool BKM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
