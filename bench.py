@@ -70,19 +70,30 @@ DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,), "profile1
 
 def measured_traffic(kernel: str):
     """Per-launch DRAM bytes of `kernel` from an ncu capture recorded under
-    profiles/, or None if there is none or the GEMM source changed since."""
-    import hashlib
+    profiles/, or None if there is none or the GEMM code changed since."""
     p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     src = os.path.join(ROOT, "perfectly_balanced_token_gb300", "csrc", "gemm.cu")
     if not (os.path.exists(p) and os.path.exists(src)):
         return None
     with open(p) as f:
         rec = json.load(f).get(kernel)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    if not rec or rec.get("gemm_cu_sha256") != sha:
+    if not rec or rec.get("gemm_cu_code_sha256") != source_digest(src):
         return None
     return rec
+
+
+def source_digest(path: str) -> str:
+    """SHA-256 of a CUDA source with its // comments and blank lines removed, so
+    that a recorded capture stays valid across comment-only edits."""
+    import hashlib
+    import re
+    lines = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            code = re.sub(r"\s*//.*$", "", line.rstrip("\n")).rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def load_peaks():
