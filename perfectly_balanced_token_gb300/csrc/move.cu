@@ -59,13 +59,24 @@ k_dispatch(Dims d, PlanPtrs p, const uint4* __restrict__ x, uint4* __restrict__ 
   if (plan_failed(p.status)) return;
   const int hv = d.H / 8;  // uint4 per row
   const int ntok = d.R * d.S;
-  for (int t = blockIdx.x; t < ntok; t += gridDim.x) {
-    const uint4* xr = x + (size_t)t * hv;
-    uint4 v[VPT];
+  // the next token's row is loaded while the current one is stored
+  int t = blockIdx.x;
+  uint4 v[VPT], nv[VPT];
+  if (t < ntok) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int a = threadIdx.x + i * kRowThreads;
-      if (a < hv) v[i] = __ldcs(xr + a);
+      if (a < hv) v[i] = __ldcs(x + (size_t)t * hv + a);
+    }
+  }
+  for (; t < ntok; t += gridDim.x) {
+    const int tn = t + gridDim.x;
+    if (tn < ntok) {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int a = threadIdx.x + i * kRowThreads;
+        if (a < hv) nv[i] = __ldcs(x + (size_t)tn * hv + a);
+      }
     }
     const int32_t* dt = p.dst + (size_t)t * d.K;
     for (int k = 0; k < d.K; ++k) {
@@ -76,6 +87,8 @@ k_dispatch(Dims d, PlanPtrs p, const uint4* __restrict__ x, uint4* __restrict__ 
         if (a < hv) __stcs(out + a, v[i]);
       }
     }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) v[i] = nv[i];
   }
 }
 
