@@ -150,6 +150,13 @@ k_scan(Dims d, PlanPtrs p) {
 // ---------------------------------------------------------------------------
 enum : int32_t { kBalanced = 0, kUnder = 1, kOver = 2 };
 
+// The plain policy's fills run in parallel when the extra shared arrays fit.
+__host__ __device__ inline bool kParallelFills(const Dims& d) { return d.policy == 0 && d.R <= 1024; }
+__host__ __device__ inline size_t plan_smem_bytes(const Dims& d) {
+  return sizeof(int32_t) * (kParallelFills(d) ? (5 * (size_t)d.E + 14 * (size_t)d.R)
+                                              : (3 * (size_t)d.E + 6 * (size_t)d.R));
+}
+
 __global__ void __launch_bounds__(1024)
 k_plan(Dims d, PlanPtrs p) {
   extern __shared__ int32_t sh[];
@@ -162,6 +169,17 @@ k_plan(Dims d, PlanPtrs p) {
   int32_t* sT256H = sT256F + d.R;   // [R] 256-row work tiles with at most 128 rows
   int32_t* sGroups = sT256H + d.R;  // [R] non-empty weight-row groups per rank
   int32_t* sPieceN = sGroups + d.R; // [E] pieces per expert so far
+  // parallel fills of the plain policy (present when kParallelFills(d))
+  int32_t* sOff = sPieceN + d.E;    // [E] copies of the higher-id experts of the same rank
+  int32_t* sNz = sOff + d.E;        // [E] non-empty higher-id experts of the same rank
+  int32_t* sGiven = sNz + d.E;      // [R] copies a rank has given so far
+  int32_t* sFU = sGiven + d.R;      // [R] fill f: receiving rank
+  int32_t* sFO = sFU + d.R;         // [R] fill f: giving rank
+  int32_t* sFD = sFO + d.R;         // [R] fill f: copies
+  int32_t* sFB = sFD + d.R;         // [R] fill f: copies its giver gave before it
+  int32_t* sFZ = sFB + d.R;         // [R] fill f: giver's non-empty experts used up before it
+  int32_t* sFS = sFZ + d.R;         // [R] fill f: copies placed (check)
+  int32_t* sNr = sFS + d.R;         // [R] distinct experts a rank received
   if (plan_failed(p.status)) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int EB = d.E + d.B;
@@ -203,9 +221,138 @@ k_plan(Dims d, PlanPtrs p) {
     atomicAdd(&sGroups[u], 1);
   };
 
+  const bool parallel_fills = kParallelFills(d);
+  if (parallel_fills) {
+    // Plain policy.  The fill sequence itself -- which rank fills which and
+    // by how much -- depends only on the loads (warp 0, ballots); where the
+    // copies come from follows without a walk: each giver's copies are taken
+    // as one sequence (its experts in descending id, inside an expert the
+    // highest ordinals first) and fill f takes the range [b_f, b_f + d_f) of
+    // its giver's sequence, b_f being what that giver gave before.  Every
+    // (fill, expert) pair then yields its piece independently.
+    const int lane = tid & 31, warp = tid >> 5, nwarp = nt >> 5;
+    const unsigned full = 0xffffffffu;
+    for (int h = tid; h < d.R; h += nt) {
+      sGiven[h] = 0;
+      sNr[h] = 0;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      int nfill = 0;
+      bool ok = true;
+      while (true) {
+        int u = -1, o = -1;
+        for (int h0 = 0; h0 < d.R && (u < 0 || o < 0); h0 += 32) {
+          const int h = h0 + lane;
+          const int st = h < d.R ? sState[h] : kBalanced;
+          const unsigned mu = __ballot_sync(full, st == kUnder), mo = __ballot_sync(full, st == kOver);
+          if (u < 0 && mu) u = h0 + __ffs(mu) - 1;
+          if (o < 0 && mo) o = h0 + __ffs(mo) - 1;
+        }
+        if (u < 0) break;
+        if (o < 0 || nfill >= d.R - 1) { ok = false; break; }
+        const int dcopies = d.C - sLoad[u];
+        if (lane == 0) {
+          sFU[nfill] = u;
+          sFO[nfill] = o;
+          sFD[nfill] = dcopies;
+          sFB[nfill] = sGiven[o];
+          sFS[nfill] = 0;
+          sGiven[o] += dcopies;
+          sLoad[u] = d.C;
+          sState[u] = kBalanced;
+          sLoad[o] -= dcopies;
+          sState[o] = sLoad[o] < d.C ? kUnder : (sLoad[o] > d.C ? kOver : kBalanced);
+        }
+        __syncwarp();
+        ++nfill;
+      }
+      if (lane == 0) {
+        if (!ok) set_error(p.status, MOONEP_ERR_INTERNAL);
+        p.counters[MOONEP_CNT_FILLS] = nfill;
+        sFZ[d.R - 1] = nfill;  // the fill count, read back below (fills < R)
+      }
+    }
+    __syncthreads();
+    if (plan_failed(p.status)) return;
+    const int F = sFZ[d.R - 1];
+    __syncthreads();
+    if (F > 0) {
+      // per giver: offsets and non-empty counts of the higher-id experts
+      for (int h = warp; h < d.R; h += nwarp) {
+        if (sGiven[h] == 0) continue;
+        int run = 0, runz = 0;
+        for (int top = (h + 1) * d.L - 1; top >= h * d.L; top -= 32) {
+          const int e = top - lane;
+          const int v = (e >= h * d.L) ? sT[e] : 0;
+          const int z = v > 0 ? 1 : 0;
+          int iv = v, iz = z;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int a = __shfl_up_sync(full, iv, off), b = __shfl_up_sync(full, iz, off);
+            if (lane >= off) { iv += a; iz += b; }
+          }
+          if (e >= h * d.L) {
+            sOff[e] = run + iv - v;
+            sNz[e] = runz + iz - z;
+          }
+          run += __shfl_sync(full, iv, 31);
+          runz += __shfl_sync(full, iz, 31);
+        }
+      }
+      __syncthreads();
+      // per fill: the giver's non-empty experts used up before it
+      for (int f = warp; f < F; f += nwarp) {
+        const int o = sFO[f], b = sFB[f];
+        int z = 0;
+        for (int e = o * d.L + lane; e < (o + 1) * d.L; e += 32) {
+          const int v = sT[e];
+          z += (v > 0 && sOff[e] + v <= b) ? 1 : 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(full, z, off);
+        if (lane == 0) sFZ[f] = z;
+      }
+      __syncthreads();
+      // every (fill, giver expert) pair with copies in the fill's range
+      for (int it = tid; it < F * d.L; it += nt) {
+        const int f = it / d.L, i = it % d.L;
+        const int o = sFO[f], u = sFU[f], b = sFB[f], dd = sFD[f];
+        const int e = (o + 1) * d.L - 1 - i;
+        const int te = sT[e], off = sOff[e];
+        const int t = min(b + dd, off + te) - max(b, off);
+        if (t <= 0) continue;
+        const int left = te - max(0, b - off);  // copies of e not yet taken
+        const int j = sNz[e] - sFZ[f];          // acquisition order within the fill
+        int pi = 0;                             // earlier fills of this giver that took from e
+        for (int f2 = 0; f2 < f; ++f2) pi += (sFO[f2] == o && sFB[f2] + sFD[f2] > off) ? 1 : 0;
+        if (pi >= d.R) { set_error(p.status, MOONEP_ERR_INTERNAL); continue; }
+        const int g = (j < d.B) ? d.E + j : e;
+        if (j < d.B) p.slot_expert[u * d.B + j] = e;
+        p.pieces[(size_t)e * d.R + pi] = Piece{left - t, left, u, g};
+        atomicAdd(&sPieceN[e], 1);
+        atomicAdd(&sMig[e], t);
+        atomicAdd(&sFS[f], t);
+        atomicAdd(&sNr[u], 1);
+        p.cu[(size_t)u * (EB + 1) + g + 1] = t;
+        count_group(u, t);
+      }
+      __syncthreads();
+      for (int f = tid; f < F; f += nt) {
+        const int u = sFU[f];
+        p.fills[3 * f + 0] = u;
+        p.fills[3 * f + 1] = sFO[f];
+        p.fills[3 * f + 2] = sFD[f];
+        p.src[u] = sFO[f];
+        p.n_recv[u] = sNr[u];
+        if (sFS[f] != sFD[f] || (d.mode == 0 && sNr[u] > d.B)) set_error(p.status, MOONEP_ERR_INTERNAL);
+      }
+    }
+  }
+
   // the fills, sequential by construction (at most R-1 of them); warp 0 runs
   // them, each decision made with ballots / shuffles so all lanes agree
-  if (tid < 32) {
+  if (!parallel_fills && tid < 32) {
     const int lane = tid;
     const unsigned full = 0xffffffffu;
     int nfill = 0;
@@ -588,7 +735,7 @@ cudaError_t launch_plan(const Dims& d, const int32_t* idx, const PlanPtrs& p, cu
     if (err != cudaSuccess) return err;
   }
   k_hist<<<dim3(d.nchunk, d.R), kHistWarps * 32, hist_smem, st>>>(d, idx, p);
-  const size_t plan_smem = sizeof(int32_t) * (3 * d.E + 6 * d.R);
+  const size_t plan_smem = plan_smem_bytes(d);
   if (plan_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (err != cudaSuccess) return err;
