@@ -137,13 +137,15 @@ def workload_config(w, maxvios):
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms.  Started before the warm-up (its own
+    """nvidia-smi sampled every 50 ms.  Started before the warm-up (its own
     start-up must not overlap the timed region); summary() keeps only the
-    samples taken inside the timed window."""
+    samples taken inside the timed window (plus one sampling interval on each
+    side, so that a short window still gets a sample)."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index: int):
         self.proc = None
@@ -154,7 +156,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -184,7 +186,8 @@ class ClockSampler:
                 clk, cmax = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            if not (t0 - 0.25 <= ts <= t1 + 0.25):
+            pad = self.INTERVAL_MS / 1000.0
+            if not (t0 - pad <= ts <= t1 + pad):
                 continue
             sm.append(clk)
             mx.append(cmax)

@@ -54,3 +54,23 @@ def test_peaks_lookup_has_the_denominators():
     peaks, src = bench.load_peaks()
     assert src in ("measured", "fallback")
     assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 500
+
+
+def test_clock_summary_keeps_the_timed_window():
+    import datetime
+    cs = bench.ClockSampler(0)
+    base = datetime.datetime(2026, 1, 1, 12, 0, 0)
+
+    def line(dt_ms, mhz, cap):
+        ts = (base + datetime.timedelta(milliseconds=dt_ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+
+    # samples every 50 ms from 0 to 1000 ms; the timed window is 410..490 ms
+    cs.lines = [line(t, 1000 + t, "Active" if t == 450 else "Not Active") for t in range(0, 1001, 50)]
+    t0 = (base + datetime.timedelta(milliseconds=410)).timestamp()
+    t1 = (base + datetime.timedelta(milliseconds=490)).timestamp()
+    s = cs.summary(t0, t1)
+    assert s["samples"] == 3  # 360 .. 540 ms: one interval of slack on each side
+    assert s["sm_mhz"] == 1450
+    assert s["reasons"] == ["sw_power_cap"]
+    assert cs.summary(t1 + 10, t1 + 20) is None
