@@ -8,9 +8,10 @@ returns.
 
 Routing recipes (all seeded):
 
-* ``zipf_bias_routing`` -- router logits ~ N(0,1) plus one per-expert bias
-  drawn from Zipf(1.2); top-K distinct experts by logit; gates = softmax of the
-  chosen K logits.  This is the small smoke-sized workload.
+* ``zipf_bias_routing`` -- router logits ~ N(0,1) plus a per-expert bias
+  -1.2*log(pi(e)+1), a Zipf popularity law over a seeded permutation pi;
+  top-K distinct experts by logit; gates = softmax of the chosen K logits.
+  This is the small smoke-sized workload.
 * ``gumbel_topk_routing`` -- weighted sampling without replacement by the
   Gumbel-max trick: score_e = log w_e + Gumbel noise, w_e = (pi(e)+1)^-alpha
   with pi a seeded permutation so hot experts land on different home ranks.
@@ -65,7 +66,11 @@ def input_skew(idx: np.ndarray, E: int) -> float:
 def zipf_bias_routing(R: int, S: int, K: int, E: int, seed: int = 0,
                       zipf_a: float = 1.2) -> Routing:
     rng = np.random.default_rng(seed)
-    bias = rng.zipf(zipf_a, size=E).astype(np.float64)
+    # Zipf popularity in logit space: expert of popularity rank p gets
+    # -a*log(p+1), so popular experts win often but every token still draws
+    # its own noise (raw Zipf samples as the bias would dwarf the noise and
+    # send every token to the same K experts)
+    bias = -zipf_a * np.log(rng.permutation(E) + 1.0)
     logits = rng.standard_normal((R, S, E)) + bias
     idx = _topk_desc(logits, K)
     gates = _softmax_last(np.take_along_axis(logits, idx, axis=-1))
