@@ -59,6 +59,9 @@ def test_dims_validation():
             mx.moonep_plan_workspace_bytes(d)
         assert ei.value.status == _lib.ERR_SHAPE
     for d in [mx.dims(0, 8, 2, 2, 16, 64, 64), mx.dims(4, 8, -1, 2, 16, 64, 64, 1),
+              mx.dims(4, 8, 2, 2, 0, 64, 64), mx.dims(4, 8, 2, 0, 16, 64, 64),  # S = 0, K = 0
+              mx.dims(4, 0, 0, 2, 16, 64, 64, 1), mx.dims(4, 8, 2, 2, 16, 0, 64),
+              mx.dims(4, 8, 2, 2, 16, 64, 0),
               mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 2), mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 0, 64),
               mx.dims(4, 8, 2, 2, 16, 64, 64, 0, 0, 512)]:
         with pytest.raises(mx.MoonepError) as ei:
