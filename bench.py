@@ -396,6 +396,9 @@ def run_ours(args):
             del bwd[b_]
         torch.cuda.empty_cache()
 
+    send_once = None if args.no_send_once else time_send_once(
+        mx, torch, d, ws, w, sweep, idx, x, gates, recv, flush, args.warmup, args.steps)
+
     # e2e: host buffers through the same C ABI, copies inside the timed region
     e2e = None if args.no_e2e else run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot,
                                             g_home, g_slot, dev, st, world)
@@ -454,6 +457,7 @@ def run_ours(args):
         "planner": "Theorem 1 construction, fixed tie-break (dims.policy = 0)",
         "planner_largest_first": policy1,
         "training_step": training,
+        "send_once_dispatch": send_once,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "pages":
         result["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
@@ -462,6 +466,51 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result))
+
+
+def time_send_once(mx, torch, d, ws, w, sweep, idx, x, gates, recv, flush, warmup, steps):
+    """The send-once dispatch (send pass + receive copy) per routing, outside the
+    timed step: one CUDA graph per routing, an L2 flush before every replay,
+    CUDA events around it.  HBM bytes of the two passes on one GPU: x read once,
+    one row written per (token, destination rank) pair, each later entry for
+    the same rank read back and written again on the receiver, plus the route,
+    destination, gate reads and weight writes (16 B per entry); the bytes that
+    would cross ranks are the per-entry and send-once link figures."""
+    recv_w = torch.empty(w.N, dtype=torch.float32, device=recv.device)
+    rows = []
+    for j, mv in enumerate(sweep):
+        mx.moonep_plan(d, idx[j], ws.buf)
+        route = ws.view("route", (w.N,))
+        dups = int((route < 0).sum().item())
+        c = ws.view("counters", (8,)).cpu().tolist()
+        for _ in range(warmup):
+            mx.moonep_dispatch_send_once(d, ws.buf, x, gates[j], recv, recv_w)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            mx.moonep_dispatch_send_once(d, ws.buf, x, gates[j], recv, recv_w)
+        g.replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            evs[i][0].record()
+            g.replay()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        payload = 2 * w.H
+        hbm = w.R * w.S * payload + w.N * payload + dups * payload + 16 * w.N
+        rows.append({"maxvio_target": mv, "ms": ms, "hbm_bytes": hbm,
+                     "achieved_gbs": hbm / (ms / 1e3) / 1e9,
+                     "receiver_copies": dups,
+                     "link_bytes_per_entry": c[4] * (payload + 4),
+                     "link_bytes_send_once": c[5] * payload + c[4] * 4})
+    status = mx.moonep_read_status(d, ws.buf)
+    if status:
+        raise RuntimeError(f"device status after the send-once dispatch {status:#x}: "
+                           f"{mx.status_string(status)}")
+    return {"call": "moonep_dispatch_send_once (k_send + k_receive_copy)", "sweep": rows}
 
 
 def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_slot, dev, st,
@@ -667,6 +716,8 @@ def main(argv=None):
                     help="skip timing the largest-first planner policy")
     ap.add_argument("--no-training", action="store_true",
                     help="skip timing the training step (forward + backward)")
+    ap.add_argument("--no-send-once", action="store_true",
+                    help="skip timing the send-once dispatch")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pages",
                     help="pages = the headline configuration; the others are smaller cases "
                          "of the same kernels for profiling")
