@@ -609,7 +609,7 @@ k_tables(Dims d, PlanPtrs p) {
   int row = ra - rsum, tile = tb - tsum + p.rank_tiles[u], grp = gc - gsum + p.rank_groups[u];
   __syncthreads();  // every thread has read its rows before they are replaced
   for (int g = g0, i = 0; g < g1; ++g, ++i) {
-    const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 5 for E <= 4096
+    const int rows = (i < 8) ? rows_local[i] : 0;  // per <= 8: E + B <= 2 * 4096
     cu[g] = row;
     const int wsel = (g < d.E) ? g : -1 - (u * d.B + (g - d.E));
     for (int m = 0; m * tile_m < rows; ++m) {

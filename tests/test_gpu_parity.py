@@ -160,6 +160,48 @@ def _layer_parity(name, w, rt, gemm_rows):
     return run
 
 
+# the largest sizes the planner accepts: E = 4096 (its shared-memory
+# histograms), R = 1024 (the most ranks the parallel-fill path takes) and
+# R = 2048 (past it: the one-warp fill loop), each under both planner policies
+MAX_CASES = [
+    ("max-e4096", W("maxE", R=8, E=4096, B=512, K=8, S=256, H=64, Hp=64),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=14)),
+    ("max-r1024", W("maxR1k", R=1024, E=4096, B=4, K=2, S=8, H=64, Hp=64),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.5, seed=15)),
+    ("max-r2048", W("maxR2k", R=2048, E=4096, B=2, K=2, S=4, H=64, Hp=64),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.5, seed=16)),
+]
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+@pytest.mark.parametrize("name,w,mk", MAX_CASES, ids=[c[0] for c in MAX_CASES])
+def test_maximum_sizes(name, w, mk, policy):
+    """Plan tables and route entries bit-exact, dispatch byte-exact, GEMM and
+    combine within tolerance, at the planner's size limits."""
+    rt = mk(w)
+    od = gh.odims(w, policy)
+    fp = oplanner.full_plan(rt.idx, od)
+    assert fp["n_fills"] > 0
+    run = gh.Run(w, rt, policy=policy)
+    run.forward()
+    tabs = run.ws.tables()
+    gh.compare_plan(tabs, fp, od)
+    assert np.array_equal(tabs["route"], oplanner.route_encoding(fp["dst"], od))
+    x_bits, w_bits = gh.host_bits(run.x), gh.host_bits(run.w_home)
+    assert np.array_equal(gh.host_bits(run.recv).reshape(w.N, w.H),
+                          olayer.permute(x_bits, fp["dst"], od))
+    per_e = olayer.expert_outputs(x_bits, w_bits, rt.idx, od)
+    y = gh.bf16_to_np(run.y).reshape(w.N, w.Hp)
+    dst = fp["dst"].reshape(-1)
+    for e, (cids, yb) in per_e.items():
+        if cids.size:
+            gh.assert_close(y[dst[cids]], gh.bits_to_np(yb), f"{name} Y expert {e}")
+    out_want = olayer.combine_from_copies(per_e, rt.gates, od)
+    gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(out_want),
+                    f"{name} combine")
+    run.check_all_guards()
+
+
 @pytest.mark.parametrize("name,w,mk", CASES[:6], ids=[c[0] for c in CASES[:6]])
 def test_gemm_isolated_synthetic_rows(name, w, mk):
     """GEMM on a synthetic receive buffer (not produced by dispatch)."""
