@@ -646,7 +646,6 @@ class OracleSample:
         oplanner.full_plan(self.rt.idx, self.od)
         t_plan = time.perf_counter() - t0
         rng = np.random.default_rng(self.seed)
-        flat = self.rt.idx.reshape(-1)
         copies, t_rest, experts = 0, 0.0, []
         while t_plan + t_rest < budget_s and len(experts) < w.E:
             e = int(rng.integers(0, w.E))
@@ -654,11 +653,14 @@ class OracleSample:
                 continue
             experts.append(e)
             wb = syn.bf16_bits(syn.normal_bf16((w.H, w.Hp), 0.02, 100 + e, "cpu"))
-            cids = np.nonzero(flat == e)[0]
             t1 = time.perf_counter()
-            rows = olayer.bf16_to_f64(self.x[cids // w.K])                  # permute (gather)
-            yb = olayer.to_bf16(rows @ olayer.bf16_to_f64(wb))              # expert GEMM
-            g = self.rt.gates.reshape(-1)[cids].astype(np.float64)[:, None]  # combine share
+            # the oracle's own per-expert step: gather the copies' token rows
+            # (permute) and multiply by the expert's weights
+            cids, yb = olayer.expert_outputs(self.x, lambda _e: wb, self.rt.idx, self.od,
+                                             experts=[e])[e]
+            # combine's share for these copies: the oracle's fp64 gate-weighted
+            # accumulation and bf16 rounding (combine itself needs every copy)
+            g = self.rt.gates.reshape(-1)[cids].astype(np.float64)[:, None]
             olayer.to_bf16(g * olayer.bf16_to_f64(yb))
             t_rest += time.perf_counter() - t1
             copies += cids.size
