@@ -154,3 +154,13 @@ def test_binding_requires_cuda_tensors():
     with pytest.raises(ValueError):
         mx.moonep_plan(d, torch.zeros(4 * 16 * 2, dtype=torch.int32),
                        torch.zeros(mx.moonep_plan_workspace_bytes(d), dtype=torch.uint8))
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    # no fallback: with the shared library absent the first call raises
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", "/nonexistent/libmoonep.so")
+    with pytest.raises(ImportError):
+        _lib.library()
+    with pytest.raises(ImportError):
+        mx.moonep_plan_workspace_bytes(mx.dims(4, 8, 2, 2, 16, 64, 64))
