@@ -164,3 +164,49 @@ def test_missing_library_fails_loudly(monkeypatch):
         _lib.library()
     with pytest.raises(ImportError):
         mx.moonep_plan_workspace_bytes(mx.dims(4, 8, 2, 2, 16, 64, 64))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moonep.h"
+
+int main(void) {
+  moonep_dims d;
+  size_t bytes = 0;
+  moonep_plan_layout lay;
+  memset(&d, 0, sizeof d);
+  d.R = 8; d.E = 384; d.B = 48; d.K = 8; d.S = 8192; d.H = 7168; d.Hp = 2048;
+  if (moonep_plan_workspace_bytes(&d, &bytes) != MOONEP_OK || bytes == 0) return 1;
+  const size_t total = bytes;
+  if (moonep_get_plan_layout(&d, &lay) != MOONEP_OK || lay.total_bytes != total) return 2;
+  if (lay.cu_seqlens % 256 != 0 || lay.dst % 256 != 0 || lay.route + 4 > total) return 3;
+  d.B = 47; /* training needs B >= E/R */
+  if (moonep_plan_workspace_bytes(&d, &bytes) != MOONEP_ERR_SLOTS) return 4;
+  if (moonep_plan_workspace_bytes(NULL, &bytes) != MOONEP_ERR_ARG) return 5;
+  if (strlen(moonep_status_string(MOONEP_ERR_ROUTING)) == 0) return 6;
+  printf("%zu\n", total);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path, lib):
+    # a C99 program against the public header and the shared library alone
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from perfectly_balanced_token_gb300.build import LIB
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        str(src), LIB, f"-Wl,-rpath,{os.path.dirname(LIB)}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    total = mx.moonep_plan_workspace_bytes(mx.dims(8, 384, 48, 8, 8192, 7168, 2048))
+    assert r.stdout.split()[0] == str(total)
