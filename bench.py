@@ -149,17 +149,32 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
+        self.reader = None
         self.gpu = gpu_index
         self.lines = []
 
+    def command(self):
+        return ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)]
+
     def start(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(self.command(), stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # drain the pipe as lines arrive: a full pipe would stall the sampler
+        # long before a multi-minute run ends
+        self.reader = threading.Thread(target=self._drain, args=(self.proc.stdout,), daemon=True)
+        self.reader.start()
+
+    def _drain(self, pipe):
+        for line in pipe:
+            line = line.strip()
+            if line:
+                self.lines.append(line)
 
     def stop(self):
         if self.proc is None:
@@ -167,11 +182,11 @@ class ClockSampler:
         time.sleep(0.3)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        self.lines = out.strip().splitlines()
+            self.proc.wait()
+        self.reader.join(timeout=5)
         self.proc = None
 
     def summary(self, t0: float, t1: float):

@@ -76,6 +76,32 @@ def test_clock_summary_keeps_the_timed_window():
     assert cs.summary(t1 + 10, t1 + 20) is None
 
 
+def test_clock_sampler_drains_its_pipe_while_running():
+    # a sampler that writes far more than a pipe buffer before it is stopped
+    # must neither stall nor lose lines: the reader thread keeps up
+    import sys
+
+    class Fake(bench.ClockSampler):
+        def command(self):
+            code = ("import sys, time\n"
+                    "for i in range(4000):\n"
+                    "    sys.stdout.write('%06d' % i + ',' + 'x' * 120 + '\\n')\n"
+                    "sys.stdout.flush()\n"
+                    "time.sleep(30)\n")
+            return [sys.executable, "-c", code]
+
+    cs = Fake(0)
+    cs.start()
+    import time
+    deadline = time.time() + 20
+    while len(cs.lines) < 4000 and time.time() < deadline:
+        time.sleep(0.05)
+    cs.stop()
+    assert len(cs.lines) == 4000  # ~500 KB went through while the process kept running
+    assert cs.lines[0].startswith("000000,") and cs.lines[-1].startswith("003999,")
+    assert cs.summary(0.0, 1.0) is None  # not nvidia-smi lines: nothing to summarise
+
+
 def test_reference_arm_prints_one_contract_line():
     # the reference arm times the oracle on the host cores: one JSON line with
     # the same metric and config as the GPU arm, and no GPU work at all
