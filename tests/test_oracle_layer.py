@@ -2,7 +2,6 @@
 import os
 
 import numpy as np
-import pytest
 
 from oracle import layer, planner
 from oracle.planner import Dims

@@ -15,7 +15,6 @@ import json
 import os
 import types
 
-import numpy as np
 import pytest
 
 from oracle import layer, planner, theory
