@@ -210,3 +210,36 @@ def test_header_is_plain_c_and_links(tmp_path, lib):
     assert r.returncode == 0, (r.returncode, r.stderr)
     total = mx.moonep_plan_workspace_bytes(mx.dims(8, 384, 48, 8, 8192, 7168, 2048))
     assert r.stdout.split()[0] == str(total)
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    # field offsets and sizes of the ctypes structures equal the C compiler's
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"moonep_dims": _lib.moonep_dims, "moonep_plan_layout": _lib.moonep_plan_layout}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moonep.h"', 'int main(void) {']
+    for sname, cls in structs.items():
+        lines.append(f'  printf("{sname} sizeof %zu\\n", sizeof({sname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{sname} {fname} %zu\\n", offsetof({sname}, {fname}));')
+    lines += ['  return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([cc, "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60).stdout.split("\n")
+    got = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in out if ln.strip()}
+    for sname, cls in structs.items():
+        assert got[(sname, "sizeof")] == ctypes.sizeof(cls), sname
+        for fname, _ in cls._fields_:
+            assert got[(sname, fname)] == getattr(cls, fname).offset, (sname, fname)
+    # and every field the header declares is in the binding
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct moonep_plan_layout \{(.*?)\}", text, flags=re.S).group(1)
+    declared = re.findall(r"\b(\w+)\s*;", body)
+    assert declared == [f for f, _ in _lib.moonep_plan_layout._fields_]
