@@ -11,7 +11,8 @@ Routing recipes (all seeded):
 * ``zipf_bias_routing`` -- router logits ~ N(0,1) plus a per-expert bias
   -1.2*log(pi(e)+1), a Zipf popularity law over a seeded permutation pi;
   top-K distinct experts by logit; gates = softmax of the chosen K logits.
-  This is the small smoke-sized workload.
+  This is the small smoke-sized workload; ``zipf_sample_bias_routing`` keeps
+  the literal form with raw Zipf(1.2) samples as the bias.
 * ``gumbel_topk_routing`` -- weighted sampling without replacement by the
   Gumbel-max trick: score_e = log w_e + Gumbel noise, w_e = (pi(e)+1)^-alpha
   with pi a seeded permutation so hot experts land on different home ranks.
@@ -71,6 +72,20 @@ def zipf_bias_routing(R: int, S: int, K: int, E: int, seed: int = 0,
     # its own noise (raw Zipf samples as the bias would dwarf the noise and
     # send every token to the same K experts)
     bias = -zipf_a * np.log(rng.permutation(E) + 1.0)
+    logits = rng.standard_normal((R, S, E)) + bias
+    idx = _topk_desc(logits, K)
+    gates = _softmax_last(np.take_along_axis(logits, idx, axis=-1))
+    return Routing(idx.astype(np.int32), gates.astype(np.float32))
+
+
+def zipf_sample_bias_routing(R: int, S: int, K: int, E: int, seed: int = 0,
+                             zipf_a: float = 1.2) -> Routing:
+    """The literal form of the small recipe: raw Zipf(zipf_a) samples as the
+    per-expert bias.  Their heavy tail usually dwarfs the N(0,1) noise, so every
+    token picks the same K experts: a degenerate but valid routing (kept as a
+    parity case of its own)."""
+    rng = np.random.default_rng(seed)
+    bias = rng.zipf(zipf_a, size=E).astype(np.float64)
     logits = rng.standard_normal((R, S, E)) + bias
     idx = _topk_desc(logits, K)
     gates = _softmax_last(np.take_along_axis(logits, idx, axis=-1))

@@ -63,6 +63,9 @@ CASES = [
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=0.8, seed=10)),
     ("bn256-infer-overflow", W("bn256i", R=4, E=16, B=1, K=2, S=300, H=128, Hp=1024, mode=1),
      lambda w: syn.round_robin_routing(w.R, w.S, w.K, w.E, first=4)),
+    # the small recipe's literal form, raw Zipf samples as the bias: every
+    # token on the same two experts
+    ("tiny-raw-zipf-bias", syn.TINY, lambda w: syn.zipf_sample_bias_routing(w.R, w.S, w.K, w.E, 0)),
 ]
 
 
