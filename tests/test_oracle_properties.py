@@ -12,11 +12,14 @@ group; and the send-once route entries decode back to the destinations with
 one payload-carrying entry per (token, destination rank) (section 在线规划、
 零拷贝、静态 shape).  On the tiniest draws the planner's largest per-rank
 redundant count is compared with the exact minimax found by brute force.
+On the same draws the plan-driven layer (permute, grouped GEMM over the
+[E+B, H, H'] rows, combine, reduce_grad) is checked against its plan-free
+definitions: a plan changes where a copy is computed, never its result.
 """
 import numpy as np
 import pytest
 
-from oracle import planner, theory
+from oracle import layer, planner, theory
 from oracle.planner import Dims
 from tests.invariants import check_plan_arrays
 
@@ -76,11 +79,47 @@ def _check(case):
         assert m is not None and m <= int(fp["n_recv"].max(initial=0))
 
 
+def _check_layer(case):
+    """Whatever the plan, the plan-driven layer equals the plan-free one: the
+    grouped GEMM over each rank's buffer gives every copy bf16(x W_e), the
+    combine equals the per-copy definition, and reduce_grad conserves the sum
+    of home and slot gradients (small integers, so exactly)."""
+    d0, idx = case
+    rng = np.random.default_rng(int(idx.sum()) + d0.R)
+    d = Dims(R=d0.R, E=d0.E, B=d0.B, K=d0.K, S=d0.S, H=8, Hp=5, mode=d0.mode, policy=d0.policy)
+    x = layer.to_bf16(rng.integers(-3, 4, size=(d.R, d.S, d.H)).astype(np.float64))
+    w = layer.to_bf16(rng.integers(-3, 4, size=(d.E, d.H, d.Hp)).astype(np.float64))
+    gates = rng.random((d.R, d.S, d.K)).astype(np.float32)
+    fp = planner.full_plan(idx, d)
+    y_rows = layer.grouped_gemm_rows(layer.permute(x, fp["dst"], d), fp["plan"], w)
+    per_e = layer.expert_outputs(x, w, idx, d)
+    dst = fp["dst"].reshape(-1)
+    for e, (cids, yb) in per_e.items():
+        assert np.array_equal(y_rows[dst[cids]], yb)
+    assert np.array_equal(layer.combine(y_rows, fp["dst"], gates, d),
+                          layer.combine_from_copies(per_e, gates, d))
+    if d.B:
+        gh = rng.integers(-9, 10, size=(d.E, 2, 3)).astype(np.float32)
+        gs = rng.integers(-9, 10, size=(d.R, d.B, 2, 3)).astype(np.float32)
+        gs[fp["slot_expert"] < 0] = 0.0
+        total = gh.astype(np.float64).sum() + gs.astype(np.float64).sum()
+        layer.reduce_grad(gh, gs, fp["plan"])
+        assert np.all(gs == 0.0) and gh.astype(np.float64).sum() == total
+
+
 if hyp is not None:
     @hyp.settings(max_examples=400, deadline=None)
     @hyp.given(st.composite(_case)())
     def test_plan_properties_on_arbitrary_small_shapes(case):
         _check(case)
+
+    @hyp.settings(max_examples=150, deadline=None)
+    @hyp.given(st.composite(_case)())
+    def test_layer_is_plan_independent_on_arbitrary_small_shapes(case):
+        _check_layer(case)
 else:
     def test_plan_properties_on_arbitrary_small_shapes():
+        pytest.skip("hypothesis is not installed")
+
+    def test_layer_is_plan_independent_on_arbitrary_small_shapes():
         pytest.skip("hypothesis is not installed")
