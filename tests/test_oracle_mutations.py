@@ -85,6 +85,27 @@ MUTANTS = [
      [("remote = [u for u in ranks if u != r]", "remote = ranks")],
      [tp.test_route_encoding_hand_case]),
     # ---- planner: the largest-first policy ----
+    ("largest-first-smallest-surplus", "planner",
+     [("o = max(over, key=lambda h: (load[h] - C, -h))", "o = min(over, key=lambda h: (load[h] - C, h))")],
+     _hand("r4e4k1s6-largest-first-pairing")),
+    ("largest-first-smallest-deficit", "planner",
+     [("u = min(under, key=lambda h: (load[h] - C, h))", "u = max(under, key=lambda h: (load[h] - C, -h))")],
+     _hand("r4e4k1s6-largest-first-pairing")),
+    ("largest-first-u-by-smallest-id", "planner",
+     [("u = min(under, key=lambda h: (load[h] - C, h))", "u = under[0]")],
+     _hand("r4e4k1s6-largest-first-pairing")),
+    ("largest-first-o-by-smallest-id", "planner",
+     [("o = max(over, key=lambda h: (load[h] - C, -h))", "o = over[0]")],
+     _hand("r4e4k1s6-largest-first-pairing")),
+    ("largest-first-deficit-ties-to-largest-id", "planner",
+     [("u = min(under, key=lambda h: (load[h] - C, h))", "u = min(under, key=lambda h: (load[h] - C, -h))")],
+     _hand("r4e4k1s5-largest-first-ties")),
+    ("largest-first-surplus-ties-to-largest-id", "planner",
+     [("o = max(over, key=lambda h: (load[h] - C, -h))", "o = max(over, key=lambda h: (load[h] - C, h))")],
+     _hand("r4e4k1s5-largest-first-ties")),
+    ("largest-first-expert-ties-to-lowest-id", "planner",
+     [("left, e = max(cand)", "left, e = max(cand, key=lambda c: (c[0], -c[1]))")],
+     _hand("r3e6k1s8-largest-first-expert-choice")),
     ("largest-first-takes-highest-id", "planner",
      [("left, e = max(cand)", "left, e = max(cand, key=lambda c: (c[0] > 0, c[1]))")],
      _seeds(tp.test_largest_first_each_fill_uses_the_fewest_experts, range(10))),
