@@ -126,23 +126,32 @@ def _check_reduce_sample(run, fp, w, rng, n_exp=6):
     del g_home, g_slot
 
 
+# every routing the benchmark times, under the planner policy it times it with:
+# the pages shape at maxvio 0.2, 1, 10 and 20 and the K3 shape at maxvio 1 and
+# 10 with the plain policy; the largest-first policy at the most skewed routing
+# of each shape
 LARGE = [
-    ("pages-maxvio1", syn.PAGES, 1.0),
-    ("pages-maxvio20", syn.PAGES, 20.0),
-    ("k3-maxvio10", syn.K3, 10.0),
+    ("pages-maxvio0.2", syn.PAGES, 0.2, 0),
+    ("pages-maxvio1", syn.PAGES, 1.0, 0),
+    ("pages-maxvio10", syn.PAGES, 10.0, 0),
+    ("pages-maxvio20", syn.PAGES, 20.0, 0),
+    ("k3-maxvio1", syn.K3, 1.0, 0),
+    ("k3-maxvio10", syn.K3, 10.0, 0),
+    ("pages-maxvio20-largest-first", syn.PAGES, 20.0, 1),
+    ("k3-maxvio10-largest-first", syn.K3, 10.0, 1),
 ]
 
 
-@pytest.mark.parametrize("name,w,mv", LARGE, ids=[c[0] for c in LARGE])
-def test_full_size_parity(name, w, mv):
+@pytest.mark.parametrize("name,w,mv,policy", LARGE, ids=[c[0] for c in LARGE])
+def test_full_size_parity(name, w, mv, policy):
     _free()
     rng = np.random.default_rng(0)
     rt = syn.routing_for(w, mv, seed=0)
-    fp = oplanner.full_plan(rt.idx, gh.odims(w))
-    run = gh.Run(w, rt, guard=1 << 16)
+    fp = oplanner.full_plan(rt.idx, gh.odims(w, policy))
+    run = gh.Run(w, rt, guard=1 << 16, policy=policy)
     run.forward()
     assert mx.moonep_read_status(run.d, run.ws.buf) == 0
-    gh.compare_plan(run.ws.tables(), fp, gh.odims(w))
+    gh.compare_plan(run.ws.tables(), fp, gh.odims(w, policy))
     _check_full_dispatch_and_prefetch(run, fp, w)
     _check_gemm_sample(run, fp, rt, w, rng)
     run.check_all_guards()
