@@ -87,7 +87,9 @@ typedef struct moonep_plan_layout {
   size_t total_bytes;
   size_t status;       /* int32[1]   sticky device status word                   */
   size_t counters;     /* int32[8]   n_fills, n_mtiles, n_occupied, n_reduce ... */
-  size_t counts;       /* int32[R][nchunk][E] per-chunk counts, then bases       */
+  size_t counts;       /* internal: int32[R][nchunk][E] per-chunk counts, then
+                          bases (planner scratch; moonep_plan_noalloc leaves it
+                          unwritten, so read T and load for the counts)     */
   size_t T;            /* int32[E]   copies routed to each expert                */
   size_t load;         /* int32[R]   copies routed to each home rank's experts   */
   size_t keep;         /* int32[E]   copies of e computed on its home rank       */
@@ -303,9 +305,12 @@ int moonep_selftest_bounded_wait(int32_t* dev_status, uint32_t limit_us, int32_t
  * cudaMalloc, cudaFree or allocating library routine).
  *
  * Arguments are those of moonep_plan; plan_ws still receives every output
- * table (its internal scratch regions are left untouched).  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
+ * table (its internal scratch regions, `counts` among them, are left
+ * untouched).  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current and keeps it for
+ * the life of the process; make that first call before any stream capture.
+ * A cudaDeviceReset of that device invalidates the kept address, so this
+ * entry point must not be called on a device after it has been reset.
  * Every call shares the one array, which keeps the last call's contents:
  * calls whose kernels overlap on the GPU (two streams, or two host threads)
  * race on it and must be serialised by the caller.  Every scratch entry a
