@@ -109,16 +109,22 @@ def test_reference_arm_prints_one_contract_line():
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+    import time
+    t0 = time.time()
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
                         "--warmup", "3", "--cpu-budget-s", "2"], cwd=root, capture_output=True,
                        text=True, timeout=600)
+    elapsed = time.time() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
     assert d["value"] > 0 and d["higher_is_better"] is True and d["gpu_launches"] == 0
-    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
+    # ms_per_step is a measured sample time, not an extrapolation: the steps it
+    # claims fit inside the process's own run
+    assert 0 < d["steps"] * d["ms_per_step"] / 1e3 <= d["wall_s_timed_region"] <= elapsed
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
