@@ -85,7 +85,9 @@ enum moonep_status {
  * Integer tables are int32 unless noted. */
 typedef struct moonep_plan_layout {
   size_t total_bytes;
-  size_t status;       /* int32[1]   sticky device status word                   */
+  size_t status;       /* int32[1]   sticky device status word; it opens a 256-byte
+                          header (status, counters, internal GEMM work-item
+                          counters) that moonep_plan zeroes                  */
   size_t counters;     /* int32[8]   n_fills, n_mtiles, n_occupied, n_reduce ... */
   size_t counts;       /* internal: int32[R][nchunk][E] per-chunk counts, then
                           bases (planner scratch; moonep_plan_noalloc leaves it

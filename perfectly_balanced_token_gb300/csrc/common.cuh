@@ -17,6 +17,11 @@ constexpr int kMmaM = 128;          // rows of one tcgen05.mma (cta_group::1)
 // flop); smaller groups use 128-row tiles, which keep fewer groups' weights in
 // flight at once and so hit L2 more often.
 constexpr int kHistWarps = 8;
+// Tensor-map scratch of the grouped weight-gradient kernel: per CTA, a ring of
+// kTmapSlots pairs of 128-byte tensor maps (recv and dY views whose row extent
+// ends at the current group's end); sized for up to kMaxGemmCtas CTAs.
+constexpr int kMaxGemmCtas = 256;
+constexpr int kTmapSlots = 8;
 
 // Per-expert migrated range of global ordinals [lo, hi) and where it goes.
 struct Piece {
@@ -58,6 +63,9 @@ struct PlanPtrs {
   MTile* mtiles;        // [max_mtiles]
   int32_t* rank_groups; // [R+1] group offset of each rank
   MTile* groups;        // [max_groups] non-empty (rank, weight row) groups: all rows of each
+  uint8_t* tmaps;       // [kMaxGemmCtas][kTmapSlots][2] tensor maps, 128 B each, GEMM scratch
+  int32_t* sched;       // [4] work-item counters of the CTA-pair GEMMs, in the zeroed header:
+                        // {pair GEMM next item, its finished pairs, dW next item, finished}
 };
 
 struct Dims {
@@ -71,7 +79,7 @@ struct Dims {
 struct Layout {
   moonep_plan_layout pub;
   size_t pieces, piece_n, piece_base, home_base, red_slots, red_n, red_list, rank_tiles,
-      rank_groups;
+      rank_groups, tmaps;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -680,6 +680,119 @@ __device__ __forceinline__ void umma_commit_pair_self(uint32_t bar) {
                : "memory");
 }
 
+// Bounded wait with cluster-scope acquire, for barriers the other CTA of the
+// pair arrives on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+// ---- work items of a CTA pair, claimed in order -------------------------------
+// The pair's leader claims work items one at a time from a counter in global
+// memory and hands each to every role of both CTAs through a ring of kQueue
+// shared-memory slots; -1 ends the sequence.  Claiming in order keeps the
+// items that run at the same time contiguous in the work order (they share
+// operand rows and weight panels in L2) and lets a pair that runs a little
+// faster take more items: with a fixed stride the pairs drifted apart by the
+// small, persistent speed differences between SMs (measured: about 1 % between
+// the slowest and the fastest pairs, over two items of spread by the end of a
+// pages-shaped forward GEMM).  The last pair to finish resets the counters for
+// the next launch; the plan also zeroes them.
+constexpr int kQueue = 16;
+constexpr int kQueueConsumers = 10;  // leader: MMA, 4 epilogue warps; peer: producer, 4 epilogue warps
+
+struct PairQueue {
+  uint32_t full0;   // this CTA's slot-0 "item written" barrier; slot s at full0 + 8 s
+  uint32_t empty0;  // this CTA's slot-0 "item read" barrier (used in the leader)
+  int32_t* items;   // this CTA's kQueue item slots
+  __device__ uint32_t full(int s) const { return full0 + 8u * s; }
+  __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+};
+
+__device__ __forceinline__ void queue_init(const PairQueue& q) {
+  for (int s = 0; s < kQueue; ++s) {
+    mbar_init(q.full(s), 1);
+    mbar_init(q.empty(s), kQueueConsumers);
+  }
+}
+
+// leader producer: the i-th claimed item t (or -1) into slot i % kQueue of both CTAs
+__device__ __forceinline__ bool queue_push(const PairQueue& q, int i, int t,
+                                           volatile int* abort_flag) {
+  const int s = i % kQueue;
+  if (!mbar_wait_cluster(q.empty(s), ((i / kQueue) & 1) ^ 1u, abort_flag)) return false;
+  q.items[s] = t;
+  const uint32_t remote = pair_map(smem_u32(q.items + s), 1);
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(t) : "memory");
+  mbar_arrive(q.full(s));
+  mbar_arrive_remote(pair_map(q.full(s), 1));
+  return true;
+}
+
+// a consumer thread (lane 0 of its role, or every lane of a warp with
+// `arrive` on lane 0 only): the i-th item, then the slot released
+__device__ __forceinline__ bool queue_take(const PairQueue& q, int i, bool leader, bool arrive,
+                                           int& t, volatile int* abort_flag) {
+  const int s = i % kQueue;
+  if (!mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)) return false;
+  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
+  if (arrive) {
+    if (leader)
+      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
+                   : "memory");
+    else
+      mbar_arrive_remote(pair_map(q.empty(s), 0));
+  }
+  return true;
+}
+
+// a whole warp takes the i-th item; lane 0 releases the slot once every lane
+// has read it
+__device__ __forceinline__ bool queue_take_warp(const PairQueue& q, int i, bool leader, int& t,
+                                                volatile int* abort_flag) {
+  const int s = i % kQueue;
+  if (!__all_sync(0xffffffffu, mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)))
+    return false;
+  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (leader)
+      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
+                   : "memory");
+    else
+      mbar_arrive_remote(pair_map(q.empty(s), 0));
+  }
+  return true;
+}
+
+// leader producer, once its pair has claimed past the end: the last pair of
+// the launch resets the counters
+__device__ __forceinline__ void queue_finish(int32_t* next, int32_t* finished, int pairs) {
+  __threadfence();
+  if (atomicAdd(finished, 1) == pairs - 1) {
+    __threadfence();
+    atomicExch(next, 0);
+    atomicExch(finished, 0);
+  }
+}
+
 // Ring depth of the pair kernel (32 KiB stages).  Measured at the pages shape:
 // 4 stages 10.0 ms, 5 stages 9.0 ms, 6 stages 9.2 ms; the sixth stage lets the
 // CTAs run further apart and raises DRAM reads from 29 to 38-41 GB per launch.
@@ -691,7 +804,8 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
   static constexpr int kBBytes = 128 * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;  // two 128-lane x 256-column fp32 accumulators
-  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int kNumBars = 2 * STAGES + 5 + 2 * kQueue;
+  static constexpr int kBarBytes = kNumBars * 8 + 16 + 4 * kQueue;
   // 32 KiB of slack past the barriers: one CTA per SM either way, and no
   // operand read of the last stage can leave this CTA's allocation
   static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes + 32768;
@@ -709,8 +823,10 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
 // barriers; both CTAs' loads complete on the leader's full barrier; each MMA
 // commit arrives on the empty (or tfull) barrier of both CTAs; each CTA drains
 // its own 128 accumulator rows and releases them on the leader's tempty.
-// Items are the 256-row tiles of the plan times N/256 column tiles; a tile of
-// at most 128 rows leaves the second CTA's rows unused.  BKM = false: the
+// Items are the 256-row tiles of the plan times N/256 column tiles, claimed in
+// order by the pair (PairQueue); a tile of at most 128 rows leaves the second
+// CTA's rows unused, and that CTA loads no rows for it: its A box starts past
+// the end of recv, which TMA fills with zeros.  BKM = false: the
 // forward product (B = W, N-major, two 64-column panels per CTA from one 3D
 // box); BKM = true: the input gradient (B = W^T, i.e. W read K-major, 128
 // weight rows per CTA).
@@ -724,7 +840,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
-  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + Cfg::kNumBars);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -732,12 +848,14 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  const PairQueue q{bar0 + 8u * (2 * STAGES + 5), bar0 + 8u * (2 * STAGES + 5 + kQueue),
+                    (int32_t*)(tmem_slot + 2)};
   constexpr uint64_t kDrainNs = 200000000ull;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = pair_rank();
   const bool leader = crank == 0;
-  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int ncl = gridDim.x >> 1;
   if (plan_failed(p.status)) return;  // uniform over the pair: before any barrier
   if (p.counters[MOONEP_CNT_TILE_ROWS] != 2 * kMmaM) return;
   const int NT = sh.N / BN;
@@ -754,6 +872,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       mbar_init(tempty(b), 8);  // four epilogue warps in each CTA
     }
     mbar_init(drain, 1);
+    queue_init(q);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -778,12 +897,25 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = cl; t < total && ok; t += ncl) {
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (leader) {  // claim the next item for the pair
+          t = atomicAdd(p.sched, 1);
+          if (t >= total) t = -1;
+          if (!queue_push(q, i, t, abort_flag)) { ok = false; break; }
+        } else if (!queue_take(q, i, false, true, t, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (t < 0) break;
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN + (int)crank * 128;
         const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
         const int wrow = (mt.wsel >= 0 ? mt.wsel : (-1 - mt.wsel)) * sh.wrows;
-        const int row0 = mt.row0 + (int)crank * kMmaM;
+        // the second CTA's rows of a tile of at most 128 rows are unused: its
+        // box starts past the last row of A, so TMA fills it with zeros and
+        // reads nothing
+        const int row0 = (crank == 0 || mt.rows > kMmaM) ? mt.row0 + (int)crank * kMmaM : d.R * d.C;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t fb = pair_map(full(stage), 0);
@@ -798,6 +930,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      if (leader) queue_finish(p.sched, p.sched + 1, ncl);
       if (ok) {
         for (int i = 0; i < STAGES; ++i) {  // every fill released: no commit still in flight
           if (!mbar_wait(empty(stage), phase ^ 1u, nullptr)) { ok = false; break; }
@@ -822,7 +955,10 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = cl; t < total && ok; t += ncl) {
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (!queue_take(q, i, true, true, t, abort_flag)) { ok = false; break; }
+        if (t < 0) break;
         if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
@@ -857,7 +993,16 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
     const int qw = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cl; t < total; t += ncl) {
+    for (int i = 0;; ++i) {
+      int t;
+      if (!queue_take_warp(q, i, leader, t, abort_flag)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      if (t < 0) break;
       const MTile mt = p.mtiles[t / NT];
       const int n0 = (t % NT) * BN;
       const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
@@ -1165,6 +1310,328 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   }
 }
 
+// Tensor maps edited on the device: `map` (128 bytes in global memory, this
+// thread's own copy) gets a new extent for dimension 1, and the edit is made
+// visible to this thread's later TMA copies through the tensor-map proxy.
+__device__ __forceinline__ void tmap_set_dim1(void* map, int extent) {
+  asm volatile(
+      "tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"((uint64_t)map),
+      "r"(extent)
+      : "memory");
+}
+__device__ __forceinline__ void tmap_publish(void* map) {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)map)
+               : "memory");
+}
+
+// Weight gradient on CTA pairs (tcgen05 cta_group::2, M = 256 rows of H,
+// N = 256 columns of H').  Work items are (group, 256-row tile of H,
+// 256-column tile of H'), H tiles fastest.  CTA c of the pair holds H rows
+// 128c.. of the tile's A = X^T and H' columns 128c.. of its B = dY, each as
+// two 64-wide panels of 64 group rows per stage: 32 KiB per SM per stage for
+// the MMA work the single-CTA kernel feeds with 48 KiB, so the ring is six
+// stages deep in the same shared memory and a third fewer operand bytes cross
+// from L2.  Each CTA drains its own 128 x 256 accumulator into G by TMA
+// reduce-adds, as the single-CTA kernel does.
+// The 64-row block that runs past a group's end is loaded through copies of
+// the recv and dY tensor maps whose row extent ends at the group's end, so TMA
+// fills the rows past it with zeros: every block of every item then completes
+// on the leader's barrier and no block needs a shared-memory fix-up.  Each CTA
+// keeps a ring of kTmapSlots such copies in the plan workspace; a copy is
+// rewritten only after the load that used it has completed (the ring is deeper
+// than the stage ring, and a stage is refilled only once its previous load
+// has been consumed).
+constexpr int kDwPairStages = 6;
+
+template <int STAGES>
+struct GemmCfgDWPair {
+  static constexpr int kABytes = kMmaM * kBK * 2;  // 128 H rows x 64 group rows
+  static constexpr int kBBytes = 128 * kBK * 2;    // 128 H' columns x 64 group rows
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 512;            // two 128-lane x 256-column fp32 accumulators
+  static constexpr int kStageOut = 16384;          // 128 rows x 32 fp32, 128-byte swizzled
+  static constexpr int kOutBytes = 2 * kStageOut;
+  static constexpr int kNumBars = 2 * STAGES + 5 + 2 * kQueue;
+  static constexpr int kBarBytes = kNumBars * 8 + 16 + 4 * kQueue;
+  static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
+};
+static_assert(kTmapSlots > kDwPairStages, "a tensor-map copy must outlive the loads in flight");
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+k_ggemm_dw_2sm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+               const __grid_constant__ CUtensorMap tm_gh, const __grid_constant__ CUtensorMap tm_gs,
+               Dims d, PlanPtrs p) {
+  using Cfg = GemmCfgDWPair<STAGES>;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* out_stage = smem + STAGES * Cfg::kStageBytes;  // 1024-aligned
+  uint64_t* bars = (uint64_t*)(out_stage + Cfg::kOutBytes);
+  uint32_t* tmem_slot = (uint32_t*)(bars + Cfg::kNumBars);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  const PairQueue q{bar0 + 8u * (2 * STAGES + 5), bar0 + 8u * (2 * STAGES + 5 + kQueue),
+                    (int32_t*)(tmem_slot + 2)};
+  constexpr uint64_t kDrainNs = 200000000ull;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = pair_rank();
+  const bool leader = crank == 0;
+  const int ncl = gridDim.x >> 1;
+  if (plan_failed(p.status)) return;  // uniform over the pair: before any barrier
+  const int MT = d.H / (2 * kMmaM), NT = d.Hp / BN;
+  const int per_group = MT * NT;
+  const int total = p.counters[MOONEP_CNT_GROUPS] * per_group;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    queue_init(q);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_dy);
+    prefetch_tmap(&tm_gh);
+    prefetch_tmap(&tm_gs);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pair_sync();  // the peer's barriers are initialised before anything reaches them
+  const uint32_t tmem_base = *tmem_slot;
+
+  // work item t: its group, first H row and first H' column (every role of
+  // both CTAs walks the same sequence)
+  auto item = [&](int t, MTile& grp, int& m0, int& n0) {
+    grp = p.groups[t / per_group];
+    const int r = t % per_group;
+    m0 = (r % MT) * (2 * kMmaM);
+    n0 = (r / MT) * BN;
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      // this CTA's ring of tensor-map copies (recv, dY) for the blocks that
+      // run past a group's end
+      uint4* maps = reinterpret_cast<uint4*>(p.tmaps) + (size_t)blockIdx.x * kTmapSlots * 16;
+      {
+        const uint4* sx = reinterpret_cast<const uint4*>(&tm_x);
+        const uint4* sy = reinterpret_cast<const uint4*>(&tm_dy);
+        for (int i = 0; i < kTmapSlots; ++i)
+          for (int j = 0; j < 8; ++j) {
+            maps[i * 16 + j] = sx[j];
+            maps[i * 16 + 8 + j] = sy[j];
+          }
+      }
+      int stage = 0, issued = 0, slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (leader) {  // claim the next item for the pair
+          t = atomicAdd(p.sched + 2, 1);
+          if (t >= total) t = -1;
+          if (!queue_push(q, i, t, abort_flag)) { ok = false; break; }
+        } else if (!queue_take(q, i, false, true, t, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (t < 0) break;
+        MTile grp;
+        int m0, n0;
+        item(t, grp, m0, n0);
+        const int KB = (grp.rows + kBK - 1) / kBK;
+        const int hrow = m0 + (int)crank * kMmaM;  // this CTA's H rows: columns of recv
+        const int ncol = n0 + (int)crank * 128;    // this CTA's H' columns of dY
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const int r0 = grp.row0 + kb * kBK;
+          const CUtensorMap* mx = &tm_x;
+          const CUtensorMap* my = &tm_dy;
+          if (grp.rows - kb * kBK < kBK) {
+            // the group's partial last block: rows from the group's end on read as zeros
+            uint4* m = maps + slot * 16;
+            tmap_set_dim1(m, grp.row0 + grp.rows);
+            tmap_set_dim1(m + 8, grp.row0 + grp.rows);
+            tmap_publish(m);
+            tmap_publish(m + 8);
+            mx = reinterpret_cast<const CUtensorMap*>(m);
+            my = reinterpret_cast<const CUtensorMap*>(m + 8);
+            if (++slot == kTmapSlots) slot = 0;
+          }
+          // both CTAs' loads complete on the leader's full barrier
+          const uint32_t fb = pair_map(full(stage), 0);
+          if (leader) mbar_expect_tx(full(stage), 2 * Cfg::kStageBytes);
+          tma_load_3d_pair(sa, mx, fb, 0, r0, hrow / 64);
+          tma_load_3d_pair(sa + Cfg::kABytes, my, fb, 0, r0, ncol / 64);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader) queue_finish(p.sched + 2, p.sched + 3, ncl);
+      if (ok) {
+        for (int i = 0; i < STAGES; ++i) {  // every fill released: no commit still in flight
+          if (!mbar_wait(empty(stage), phase ^ 1u, nullptr)) { ok = false; break; }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) set_error(p.status, MOONEP_ERR_TIMEOUT);
+      } else {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        if (leader) {  // both CTAs' copies complete on the leader's barriers
+          for (int i = 0; i < min(issued, STAGES); ++i) {
+            if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+            mbar_wait(full(stage), phase, nullptr, kDrainNs);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader only) ----------------
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = make_idesc(2 * kMmaM, BN, true, true);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (!queue_take(q, i, true, true, t, abort_flag)) { ok = false; break; }
+        if (t < 0) break;
+        const int KB = (p.groups[t / per_group].rows + kBK - 1) / kBK;
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sw128_desc(sa + k * (kUmmaK * 128), 8192, 1024);
+            const uint64_t bd = sw128_desc(sb + k * (kUmmaK * 128), 8192, 1024);
+            umma_bf16_pair(dtm, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit_pair_both(empty(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair_both(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(p.status, MOONEP_ERR_TIMEOUT);
+        umma_commit_pair_self(drain);  // completes once every MMA issued so far is done
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5, both CTAs): G += accumulator ----------------
+    const int qw = warp & 3;
+    const bool issuer = (warp == 2 && lane == 0);
+    auto epi_bar = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    auto epi_all = [](bool pred) {
+      uint32_t r;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+          : "=r"(r)
+          : "r"((uint32_t)pred)
+          : "memory");
+      return r != 0;
+    };
+    int acc = 0, chunk = 0;
+    uint32_t acc_phase = 0;
+    for (int i = 0;; ++i) {
+      int t;
+      if (!queue_take_warp(q, i, leader, t, abort_flag)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      if (t < 0) break;
+      MTile grp;
+      int m0, n0;
+      item(t, grp, m0, n0);
+      const bool okw = mbar_wait(tfull(acc), acc_phase, abort_flag);
+      if (!epi_all(okw)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const CUtensorMap* gmap = grp.wsel >= 0 ? &tm_gh : &tm_gs;
+      const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0 + (int)crank * kMmaM;
+      const uint32_t tbase = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * BN);
+      const int rr = qw * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c, ++chunk) {
+        uint8_t* buf = out_stage + (chunk & 1) * Cfg::kStageOut;
+        if (issuer) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        epi_bar();
+        uint32_t r[32];
+        tmem_ld_x32(tbase + c * 32, r);
+        tmem_ld_wait();
+        uint4* row = reinterpret_cast<uint4*>(buf + rr * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          row[j ^ (rr & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epi_bar();
+        if (issuer) {
+          asm volatile(
+              "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+              " [%0, {%1, %2}], [%3];" ::"l"((uint64_t)gmap),
+              "r"(n0 + c * 32), "r"(grow), "r"(smem_u32(buf))
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(pair_map(tempty(acc), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (issuer) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  pair_sync();  // both CTAs done with TMEM and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+}
+
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // ever arrives on, with the same helper the GEMM pipeline uses, and must give up
 // after limit_ns, record MOONEP_ERR_TIMEOUT and return.
@@ -1337,6 +1804,30 @@ static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs&
   return cudaGetLastError();
 }
 
+// The CTA-pair weight-gradient kernel on two CTAs per co-resident cluster.
+static cudaError_t launch_pair_dw(const Dims& d, const PlanPtrs& p, const CUtensorMap& tx,
+                                  const CUtensorMap& tdy, const CUtensorMap& tgh,
+                                  const CUtensorMap& tgs, cudaStream_t st) {
+  using Cfg = GemmCfgDWPair<kDwPairStages>;
+  static int grid = 0;
+  if (grid == 0) {
+    cudaError_t e = cudaFuncSetAttribute(k_ggemm_dw_2sm<kDwPairStages>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * std::max(1, sm_count_gemm() / 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, (void*)k_ggemm_dw_2sm<kDwPairStages>, &cfg);
+    if (e != cudaSuccess) return e;
+    grid = 2 * std::max(1, ncl);
+  }
+  if (grid > kMaxGemmCtas) return cudaErrorInvalidConfiguration;  // tensor-map scratch per CTA
+  k_ggemm_dw_2sm<kDwPairStages><<<grid, kGemmThreads, Cfg::kSmem, st>>>(tx, tdy, tgh, tgs, d, p);
+  return cudaGetLastError();
+}
+
 // The two weight tensors as 2D [rows][H'] maps with a box of box_outer rows
 // (the input gradient reads them K-major).
 static bool encode_weights(const Dims& d, const void* w_home, const void* w_slot,
@@ -1447,9 +1938,18 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void*
   if (!encode_2d_f32_tile(&tgsp, slots ? g_slot : g_home, (uint64_t)d.Hp,
                           slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, (uint32_t)bn))
     return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (bn == 256 && d.H % (2 * kMmaM) == 0) {
+    // 256 x 256 work tiles on CTA pairs: each CTA loads 128 of the 256 H' columns of dY
+    CUtensorMap tdy2;
+    if (!encode_panels_3d(&tdy2, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 2))
+      return cudaErrorInvalidValue;
+    e = launch_pair_dw(d, p, tx, tdy2, tgh, tgs, st);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+  }
   const long long max_items = (long long)d.max_groups * (d.H / kMmaM) * (d.Hp / bn);
   const int grid = (int)std::min<long long>(sm_count_gemm(), std::max<long long>(1, max_items));
-  cudaError_t e;
   if (bn == 256) {
     static bool set = false;
     e = launch_cfg<GemmCfgDW<256, 4>>(k_ggemm_dw<256, 4>, set, grid, st, tx, tdy, tgh, tgs, tghp, tgsp, d, p);

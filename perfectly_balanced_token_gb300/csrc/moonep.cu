@@ -103,6 +103,7 @@ static Layout make_layout(const Dims& d) {
   p.mtiles = take(sizeof(MTile) * (size_t)d.max_mtiles);
   L.rank_groups = take(4 * (R + 1));
   p.groups = take(sizeof(MTile) * (size_t)d.max_groups);
+  L.tmaps = take((size_t)kMaxGemmCtas * kTmapSlots * 2 * 128);
   p.total_bytes = off;
   p.nchunk = d.nchunk;
   p.max_mtiles = d.max_mtiles;
@@ -114,6 +115,7 @@ static PlanPtrs resolve(const Layout& L, void* ws) {
   const moonep_plan_layout& p = L.pub;
   PlanPtrs q;
   q.status = (int32_t*)(b + p.status);
+  q.sched = (int32_t*)(b + p.status + 128);  // inside the 256-byte header the plan zeroes
   q.counters = (int32_t*)(b + p.counters);
   q.counts = (int32_t*)(b + p.counts);
   q.T = (int32_t*)(b + p.T);
@@ -140,6 +142,7 @@ static PlanPtrs resolve(const Layout& L, void* ws) {
   q.mtiles = (MTile*)(b + p.mtiles);
   q.rank_groups = (int32_t*)(b + L.rank_groups);
   q.groups = (MTile*)(b + p.groups);
+  q.tmaps = (uint8_t*)(b + L.tmaps);
   return q;
 }
 
