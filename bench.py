@@ -268,7 +268,7 @@ def run_ours(args):
         forward step is plan .. combine + reduce_grad; a training step inserts
         the backward (combine backward, the two GEMM gradients, dispatch
         backward) before reduce_grad."""
-        d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy)
+        d = mx.dims(w.R, w.E, w.B, w.K, w.S, w.H, w.Hp, w.mode, policy, args.gemm_rows)
         ws = mx.PlanWorkspace(d, device=dev)
 
         def calls(j):
@@ -765,6 +765,9 @@ def main(argv=None):
                     help="skip timing the training step (forward + backward)")
     ap.add_argument("--no-send-once", action="store_true",
                     help="skip timing the send-once dispatch")
+    ap.add_argument("--gemm-rows", type=int, choices=(0, 128, 256), default=0,
+                    help="GEMM work-tile height: 0 = chosen per plan by the cost model (the "
+                         "default), 128 or 256 = fixed (to profile one GEMM variant)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pages",
                     help="pages = the headline configuration; the others are smaller cases "
                          "of the same kernels for profiling")

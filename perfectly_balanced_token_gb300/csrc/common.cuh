@@ -64,8 +64,9 @@ struct PlanPtrs {
   int32_t* rank_groups; // [R+1] group offset of each rank
   MTile* groups;        // [max_groups] non-empty (rank, weight row) groups: all rows of each
   uint8_t* tmaps;       // [kMaxGemmCtas][kTmapSlots][2] tensor maps, 128 B each, GEMM scratch
-  int32_t* sched;       // [4] work-item counters of the CTA-pair GEMMs, in the zeroed header:
-                        // {pair GEMM next item, its finished pairs, dW next item, finished}
+  int32_t* sched;       // [6] work-item counters of the GEMMs, in the header the plan zeroes:
+                        // {next item, finished pairs} of the pair GEMM, of the pair weight
+                        // gradient, then {next item, finished CTAs} of the 128-row GEMM
 };
 
 struct Dims {

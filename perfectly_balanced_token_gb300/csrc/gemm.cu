@@ -46,13 +46,16 @@ constexpr int kUmmaK = 16;     // K of one tcgen05.mma for 16-bit inputs
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitNs = 4000000000ull;  // 4 s per barrier wait
 
+constexpr int kQueueSlots = 16;  // work-item queue depth (kQueue below)
+
 template <int BN, int STAGES>
 struct GemmCfgM128 {  // one 128-row tile, double-buffered accumulator
   static constexpr int kABytes = kMmaM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int kNumBars = 2 * STAGES + 5 + 2 * kQueueSlots;  // ring, TMEM, work-item queue
+  static constexpr int kBarBytes = kNumBars * 8 + 16 + 4 * kQueueSlots;
   static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes;
 };
 
@@ -240,6 +243,198 @@ struct BOperand {
   }
 };
 
+// ---- pair (cta_group::2) PTX ----------------------------------------------
+__device__ __forceinline__ uint32_t pair_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// the shared::cluster address of this CTA's shared-memory word `a` in CTA `rank`
+__device__ __forceinline__ uint32_t pair_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// TMA load into this CTA's shared memory, completing bytes on an mbarrier that
+// may sit in either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive once on the mbarrier at this offset in both CTAs of the pair when the
+// MMAs issued so far by this thread have completed
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_self(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// Bounded wait with cluster-scope acquire, for barriers the other CTA of the
+// pair arrives on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+// ---- work items of a CTA pair, claimed in order -------------------------------
+// The pair's leader claims work items one at a time from a counter in global
+// memory and hands each to every role of both CTAs through a ring of kQueue
+// shared-memory slots; -1 ends the sequence.  Claiming in order keeps the
+// items that run at the same time contiguous in the work order (they share
+// operand rows and weight panels in L2) and lets a pair that runs a little
+// faster take more items: with a fixed stride the pairs drifted apart by the
+// small, persistent speed differences between SMs (measured: about 1 % between
+// the slowest and the fastest pairs, over two items of spread by the end of a
+// pages-shaped forward GEMM).  The last pair to finish resets the counters for
+// the next launch; the plan also zeroes them.
+constexpr int kQueue = kQueueSlots;
+constexpr int kQueueConsumers = 10;  // leader: MMA, 4 epilogue warps; peer: producer, 4 epilogue warps
+constexpr int kQueueConsumersSolo = 5;  // a single CTA: MMA, 4 epilogue warps
+
+struct PairQueue {
+  uint32_t full0;   // this CTA's slot-0 "item written" barrier; slot s at full0 + 8 s
+  uint32_t empty0;  // this CTA's slot-0 "item read" barrier (used in the leader)
+  int32_t* items;   // this CTA's kQueue item slots
+  __device__ uint32_t full(int s) const { return full0 + 8u * s; }
+  __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+};
+
+__device__ __forceinline__ void queue_init(const PairQueue& q, int consumers = kQueueConsumers) {
+  for (int s = 0; s < kQueue; ++s) {
+    mbar_init(q.full(s), 1);
+    mbar_init(q.empty(s), consumers);
+  }
+}
+
+// leader producer: the i-th claimed item t (or -1) into slot i % kQueue of both
+// CTAs (of this CTA alone when `pair` is false: the same queue serves a
+// kernel of single-CTA work items)
+__device__ __forceinline__ bool queue_push(const PairQueue& q, int i, int t,
+                                           volatile int* abort_flag, bool pair = true) {
+  const int s = i % kQueue;
+  if (!mbar_wait_cluster(q.empty(s), ((i / kQueue) & 1) ^ 1u, abort_flag)) return false;
+  q.items[s] = t;
+  if (pair) {
+    const uint32_t remote = pair_map(smem_u32(q.items + s), 1);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(t) : "memory");
+  }
+  mbar_arrive(q.full(s));
+  if (pair) mbar_arrive_remote(pair_map(q.full(s), 1));
+  return true;
+}
+
+// a consumer thread (lane 0 of its role, or every lane of a warp with
+// `arrive` on lane 0 only): the i-th item, then the slot released
+__device__ __forceinline__ bool queue_take(const PairQueue& q, int i, bool leader, bool arrive,
+                                           int& t, volatile int* abort_flag) {
+  const int s = i % kQueue;
+  if (!mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)) return false;
+  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
+  if (arrive) {
+    if (leader)
+      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
+                   : "memory");
+    else
+      mbar_arrive_remote(pair_map(q.empty(s), 0));
+  }
+  return true;
+}
+
+// a whole warp takes the i-th item; lane 0 releases the slot once every lane
+// has read it
+__device__ __forceinline__ bool queue_take_warp(const PairQueue& q, int i, bool leader, int& t,
+                                                volatile int* abort_flag) {
+  const int s = i % kQueue;
+  if (!__all_sync(0xffffffffu, mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)))
+    return false;
+  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (leader)
+      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
+                   : "memory");
+    else
+      mbar_arrive_remote(pair_map(q.empty(s), 0));
+  }
+  return true;
+}
+
+// leader producer, once its pair has claimed past the end: the last pair of
+// the launch resets the counters
+__device__ __forceinline__ void queue_finish(int32_t* next, int32_t* finished, int pairs) {
+  __threadfence();
+  if (atomicAdd(finished, 1) == pairs - 1) {
+    __threadfence();
+    atomicExch(next, 0);
+    atomicExch(finished, 0);
+  }
+}
+
 // One 128-row tile per work item; the accumulator is double buffered so the
 // epilogue of one tile overlaps the main loop of the next.
 template <int BN, int STAGES, bool BKM>
@@ -251,7 +446,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
-  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 5);
+  uint32_t* tmem_slot = (uint32_t*)(bars + Cfg::kNumBars);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -259,6 +454,8 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  const PairQueue q{bar0 + 8u * (2 * STAGES + 5), bar0 + 8u * (2 * STAGES + 5 + kQueue),
+                    (int32_t*)(tmem_slot + 2)};  // a queue of this CTA's own (no pair)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (plan_failed(p.status)) return;  // uniform: before any barrier or allocation
@@ -277,6 +474,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
       mbar_init(tempty(b), 4);
     }
     mbar_init(drain, 1);
+    queue_init(q, kQueueConsumersSolo);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -300,7 +498,11 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        int t = atomicAdd(p.sched + 4, 1);  // claim the next item
+        if (t >= total) t = -1;
+        if (!queue_push(q, i, t, abort_flag, false)) { ok = false; break; }
+        if (t < 0) break;
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN;
         const CUtensorMap* wmap = mt.wsel >= 0 ? &tm_wh : &tm_ws;
@@ -315,6 +517,7 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      queue_finish(p.sched + 4, p.sched + 5, gridDim.x);
       if (!ok) {
         *abort_flag = 1;
         set_error(p.status, MOONEP_ERR_TIMEOUT);
@@ -332,7 +535,10 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (!queue_take(q, i, true, true, t, abort_flag)) { ok = false; break; }
+        if (t < 0) break;
         if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dtm = tmem_base + (uint32_t)(acc * BN);
@@ -363,10 +569,19 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;  // TMEM lanes 32q..32q+31 are this warp's rows
+    const int qw = warp & 3;  // TMEM lanes 32qw..32qw+31 are this warp's rows
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int i = 0;; ++i) {
+      int t;
+      if (!queue_take_warp(q, i, true, t, abort_flag)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_error(p.status, MOONEP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      if (t < 0) break;
       const MTile mt = p.mtiles[t / NT];
       const int n0 = (t % NT) * BN;
       const bool ok = mbar_wait(tfull(acc), acc_phase, abort_flag);
@@ -378,10 +593,10 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         break;
       }
       tc_fence_after();
-      const int row = q * 32 + lane;
+      const int row = qw * 32 + lane;
       const bool valid = row < mt.rows;
       uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tbase = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -603,193 +818,6 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
-  }
-}
-
-// ---- pair (cta_group::2) PTX ----------------------------------------------
-__device__ __forceinline__ uint32_t pair_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void pair_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// the shared::cluster address of this CTA's shared-memory word `a` in CTA `rank`
-__device__ __forceinline__ uint32_t pair_map(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-// TMA load into this CTA's shared memory, completing bytes on an mbarrier that
-// may sit in either CTA of the pair
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                 int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                 int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// arrive once on the mbarrier at this offset in both CTAs of the pair when the
-// MMAs issued so far by this thread have completed
-__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)0x3)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit_pair_self(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-
-// Bounded wait with cluster-scope acquire, for barriers the other CTA of the
-// pair arrives on.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort_flag) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_ns() - t0 > kWaitNs) return false;
-  }
-}
-
-// ---- work items of a CTA pair, claimed in order -------------------------------
-// The pair's leader claims work items one at a time from a counter in global
-// memory and hands each to every role of both CTAs through a ring of kQueue
-// shared-memory slots; -1 ends the sequence.  Claiming in order keeps the
-// items that run at the same time contiguous in the work order (they share
-// operand rows and weight panels in L2) and lets a pair that runs a little
-// faster take more items: with a fixed stride the pairs drifted apart by the
-// small, persistent speed differences between SMs (measured: about 1 % between
-// the slowest and the fastest pairs, over two items of spread by the end of a
-// pages-shaped forward GEMM).  The last pair to finish resets the counters for
-// the next launch; the plan also zeroes them.
-constexpr int kQueue = 16;
-constexpr int kQueueConsumers = 10;  // leader: MMA, 4 epilogue warps; peer: producer, 4 epilogue warps
-
-struct PairQueue {
-  uint32_t full0;   // this CTA's slot-0 "item written" barrier; slot s at full0 + 8 s
-  uint32_t empty0;  // this CTA's slot-0 "item read" barrier (used in the leader)
-  int32_t* items;   // this CTA's kQueue item slots
-  __device__ uint32_t full(int s) const { return full0 + 8u * s; }
-  __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
-};
-
-__device__ __forceinline__ void queue_init(const PairQueue& q) {
-  for (int s = 0; s < kQueue; ++s) {
-    mbar_init(q.full(s), 1);
-    mbar_init(q.empty(s), kQueueConsumers);
-  }
-}
-
-// leader producer: the i-th claimed item t (or -1) into slot i % kQueue of both CTAs
-__device__ __forceinline__ bool queue_push(const PairQueue& q, int i, int t,
-                                           volatile int* abort_flag) {
-  const int s = i % kQueue;
-  if (!mbar_wait_cluster(q.empty(s), ((i / kQueue) & 1) ^ 1u, abort_flag)) return false;
-  q.items[s] = t;
-  const uint32_t remote = pair_map(smem_u32(q.items + s), 1);
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(t) : "memory");
-  mbar_arrive(q.full(s));
-  mbar_arrive_remote(pair_map(q.full(s), 1));
-  return true;
-}
-
-// a consumer thread (lane 0 of its role, or every lane of a warp with
-// `arrive` on lane 0 only): the i-th item, then the slot released
-__device__ __forceinline__ bool queue_take(const PairQueue& q, int i, bool leader, bool arrive,
-                                           int& t, volatile int* abort_flag) {
-  const int s = i % kQueue;
-  if (!mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)) return false;
-  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
-  if (arrive) {
-    if (leader)
-      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
-                   : "memory");
-    else
-      mbar_arrive_remote(pair_map(q.empty(s), 0));
-  }
-  return true;
-}
-
-// a whole warp takes the i-th item; lane 0 releases the slot once every lane
-// has read it
-__device__ __forceinline__ bool queue_take_warp(const PairQueue& q, int i, bool leader, int& t,
-                                                volatile int* abort_flag) {
-  const int s = i % kQueue;
-  if (!__all_sync(0xffffffffu, mbar_wait_cluster(q.full(s), (i / kQueue) & 1, abort_flag)))
-    return false;
-  t = *reinterpret_cast<volatile int32_t*>(q.items + s);
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    if (leader)
-      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(q.empty(s))
-                   : "memory");
-    else
-      mbar_arrive_remote(pair_map(q.empty(s), 0));
-  }
-  return true;
-}
-
-// leader producer, once its pair has claimed past the end: the last pair of
-// the launch resets the counters
-__device__ __forceinline__ void queue_finish(int32_t* next, int32_t* finished, int pairs) {
-  __threadfence();
-  if (atomicAdd(finished, 1) == pairs - 1) {
-    __threadfence();
-    atomicExch(next, 0);
-    atomicExch(finished, 0);
   }
 }
 
