@@ -438,15 +438,19 @@ def run_ours(args):
     gemm_kernel = "+".join(("k_ggemm_2sm" if wide else "k_ggemm_m256") if r == 256 else "k_ggemm_m128"
                            for r in rows_chosen)
     traffic = measured_traffic(gemm_kernel) if args.workload == "pages" else None
+    occ = np.mean([c["occupied_slots"] for c in counters])
+    red = np.mean([c["reduced_experts"] for c in counters])
+    hh = w.H * w.Hp
     roofline = {"kernel": f"{gemm_kernel} (moonep_grouped_gemm)", "bound": "tensor",
                 "achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / bf16_peak, "peak_source": f"bf16_tflops ({peak_src}, burst)",
                 "traffic": traffic["bytes_per_launch"] if traffic else None,
                 "traffic_source": traffic["source"] if traffic else None,
-                "algorithmic_flops_per_launch": flops, "ms_per_launch": gemm_ms}
-    occ = np.mean([c["occupied_slots"] for c in counters])
-    red = np.mean([c["reduced_experts"] for c in counters])
-    hh = w.H * w.Hp
+                "traffic_method": traffic.get("method") if traffic else None,
+                "algorithmic_flops_per_launch": flops, "ms_per_launch": gemm_ms,
+                # recv read once, each used weight panel once, Y written once
+                "algorithmic_bytes_per_launch": float(N * w.H * 2 + (w.E + occ) * hh * 2
+                                                      + N * w.Hp * 2)}
     algo_bytes = {
         "dispatch": w.R * w.S * w.H * 2 + N * w.H * 2 + N * 4,
         "combine": N * w.Hp * 2 + N * 8 + w.R * w.S * w.Hp * 2,
