@@ -129,7 +129,11 @@ enum moonep_counter {
 };
 
 /* Size in bytes of the plan workspace for `dims` (host only, no CUDA call).
- * Returns MOONEP_ERR_* for invalid dims. */
+ * Returns MOONEP_ERR_* for invalid dims.  Its last MOONEP_GEMM_SCRATCH_BYTES
+ * are the grouped GEMMs' scratch: per-CTA copies of tensor maps, which hold
+ * the device addresses of the buffers the last GEMM call was given (so two
+ * otherwise identical runs on different buffers differ there). */
+#define MOONEP_GEMM_SCRATCH_BYTES (512u << 10)
 int moonep_plan_workspace_bytes(const moonep_dims* dims, size_t* bytes);
 
 /* Offsets of the workspace tables, so callers can view them (host only). */

@@ -21,6 +21,7 @@ ERR_ARG, ERR_ALIGN, ERR_SLOTS, ERR_SHAPE, ERR_CUDA, ERR_SCRATCH = 1, 2, 3, 4, 5,
 ERR_ROUTING, ERR_INTERNAL, ERR_TIMEOUT = 0x100, 0x200, 0x400
 CNT_FILLS, CNT_MTILES, CNT_OCCUPIED, CNT_REDUCE = 0, 1, 2, 3
 CNT_REMOTE_ENTRIES, CNT_REMOTE_PAIRS, CNT_GROUPS = 4, 5, 6
+GEMM_SCRATCH_BYTES = 512 << 10  # MOONEP_GEMM_SCRATCH_BYTES: the workspace's last bytes
 
 
 class MoonepError(RuntimeError):

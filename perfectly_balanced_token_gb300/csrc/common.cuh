@@ -22,6 +22,8 @@ constexpr int kHistWarps = 8;
 // ends at the current group's end); sized for up to kMaxGemmCtas CTAs.
 constexpr int kMaxGemmCtas = 256;
 constexpr int kTmapSlots = 8;
+static_assert((size_t)kMaxGemmCtas * kTmapSlots * 2 * 128 == MOONEP_GEMM_SCRATCH_BYTES,
+              "the GEMM scratch at the end of the plan workspace");
 
 // Per-expert migrated range of global ordinals [lo, hi) and where it goes.
 struct Piece {

@@ -821,6 +821,21 @@ k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   }
 }
 
+// Tensor maps edited on the device: `map` (128 bytes in global memory, this
+// thread's own copy) gets a new extent for dimension 1, and the edit is made
+// visible to this thread's later TMA copies through the tensor-map proxy.
+__device__ __forceinline__ void tmap_set_dim1(void* map, int extent) {
+  asm volatile(
+      "tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"((uint64_t)map),
+      "r"(extent)
+      : "memory");
+}
+__device__ __forceinline__ void tmap_publish(void* map) {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)map)
+               : "memory");
+}
+
 // Ring depth of the pair kernel (32 KiB stages).  Measured at the pages shape:
 // 4 stages 10.0 ms, 5 stages 9.0 ms, 6 stages 9.2 ms; the sixth stage lets the
 // CTAs run further apart and raises DRAM reads from 29 to 38-41 GB per launch.
@@ -852,9 +867,14 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
 // commit arrives on the empty (or tfull) barrier of both CTAs; each CTA drains
 // its own 128 accumulator rows and releases them on the leader's tempty.
 // Items are the 256-row tiles of the plan times N/256 column tiles, claimed in
-// order by the pair (PairQueue); a tile of at most 128 rows leaves the second
-// CTA's rows unused, and that CTA loads no rows for it: its A box starts past
-// the end of recv, which TMA fills with zeros.  BKM = false: the
+// order by the pair (PairQueue).  A group's last tile has rows past the
+// group's end; they are loaded as zeros, so the MMAs on them multiply zeros
+// (their results are never stored): a tile of at most 128 rows leaves the
+// second CTA's rows unused and that CTA's A box starts past the end of recv,
+// and a CTA whose rows run past the group's end loads them through its own
+// copy of the A tensor map with the row extent cut at the group's end (a ring
+// of kTmapSlots copies in the plan workspace, as the weight gradient uses).
+// BKM = false: the
 // forward product (B = W, N-major, two 64-column panels per CTA from one 3D
 // box); BKM = true: the input gradient (B = W^T, i.e. W read K-major, 128
 // weight rows per CTA).
@@ -922,7 +942,14 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
-      int stage = 0, issued = 0;
+      // this CTA's ring of A tensor-map copies (the first map of each slot)
+      uint4* maps = reinterpret_cast<uint4*>(p.tmaps) + (size_t)blockIdx.x * kTmapSlots * 16;
+      {
+        const uint4* sa0 = reinterpret_cast<const uint4*>(&tm_a);
+        for (int i = 0; i < kTmapSlots; ++i)
+          for (int j = 0; j < 8; ++j) maps[i * 16 + j] = sa0[j];
+      }
+      int stage = 0, issued = 0, slot = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int i = 0; ok; ++i) {
@@ -944,12 +971,21 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
         // box starts past the last row of A, so TMA fills it with zeros and
         // reads nothing
         const int row0 = (crank == 0 || mt.rows > kMmaM) ? mt.row0 + (int)crank * kMmaM : d.R * d.C;
+        const CUtensorMap* amap = &tm_a;
+        if (row0 < d.R * d.C && mt.rows < (int)(crank + 1) * kMmaM) {
+          // this CTA's rows run past the group's end: rows from there on read as zeros
+          uint4* m = maps + slot * 16;
+          tmap_set_dim1(m, mt.row0 + mt.rows);
+          tmap_publish(m);
+          amap = reinterpret_cast<const CUtensorMap*>(m);
+          if (++slot == kTmapSlots) slot = 0;
+        }
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t fb = pair_map(full(stage), 0);
           if (leader) mbar_expect_tx(full(stage), 2 * Cfg::kStageBytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes);
-          tma_load_2d_pair(sa, &tm_a, fb, kb * kBK, row0);
+          tma_load_2d_pair(sa, amap, fb, kb * kBK, row0);
           if (BKM)  // 128 weight rows (this CTA's n), 64 k each
             tma_load_2d_pair(sa + Cfg::kABytes, wmap, fb, kb * kBK, wrow + n0);
           else      // two 64-column panels of 64 k-rows
@@ -1336,21 +1372,6 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
-}
-
-// Tensor maps edited on the device: `map` (128 bytes in global memory, this
-// thread's own copy) gets a new extent for dimension 1, and the edit is made
-// visible to this thread's later TMA copies through the tensor-map proxy.
-__device__ __forceinline__ void tmap_set_dim1(void* map, int extent) {
-  asm volatile(
-      "tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"((uint64_t)map),
-      "r"(extent)
-      : "memory");
-}
-__device__ __forceinline__ void tmap_publish(void* map) {
-  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
-  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)map)
-               : "memory");
 }
 
 // Weight gradient on CTA pairs (tcgen05 cta_group::2, M = 256 rows of H,
@@ -1828,6 +1849,7 @@ static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs&
     if (e != cudaSuccess) return e;
     grid = 2 * std::max(1, ncl);
   }
+  if (grid > kMaxGemmCtas) return cudaErrorInvalidConfiguration;  // tensor-map scratch per CTA
   k_ggemm_2sm<kPairStages, BKM><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, sh, p, y);
   return cudaGetLastError();
 }

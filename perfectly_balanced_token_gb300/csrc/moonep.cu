@@ -103,7 +103,7 @@ static Layout make_layout(const Dims& d) {
   p.mtiles = take(sizeof(MTile) * (size_t)d.max_mtiles);
   L.rank_groups = take(4 * (R + 1));
   p.groups = take(sizeof(MTile) * (size_t)d.max_groups);
-  L.tmaps = take((size_t)kMaxGemmCtas * kTmapSlots * 2 * 128);
+  L.tmaps = take(MOONEP_GEMM_SCRATCH_BYTES);  // last: the layout documents it as the tail
   p.total_bytes = off;
   p.nchunk = d.nchunk;
   p.max_mtiles = d.max_mtiles;

@@ -84,6 +84,11 @@ def test_layout_tables_are_aligned_and_inside():
     for o in offs[2:]:
         assert o % 256 == 0 and o < lay.total_bytes
     assert lay.nchunk == 4 and lay.max_mtiles >= d.N // 128
+    # the GEMMs' scratch is the workspace's tail, past every table
+    assert max(offs) + 4 <= lay.total_bytes - mx.GEMM_SCRATCH_BYTES
+    hdr = open(HEADER).read()
+    m = re.search(r"#define MOONEP_GEMM_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m and int(m.group(1)) << int(m.group(2)) == mx.GEMM_SCRATCH_BYTES
 
 
 def test_bad_pointers_rejected_before_launch(lib):
