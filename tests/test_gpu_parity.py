@@ -342,3 +342,44 @@ def test_largest_first_policy_parity(name, w, mk):
     gh.assert_close(gh.bf16_to_np(run.out).reshape(w.R * w.S, w.Hp), gh.bits_to_np(out_want),
                     f"{name} combine (policy 1)")
     run.check_all_guards()
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+def test_gemm_launches_repeated_on_one_plan(rows):
+    """The GEMM kernels claim their work items from counters in the plan
+    workspace, which each launch's last CTA resets for the next: repeated
+    launches on one plan compute the same output, and two weight-gradient
+    launches add exactly twice."""
+    w = syn.SMALL
+    rt = syn.routing_for(w, 5.0)
+    od = gh.odims(w)
+    fp = oplanner.full_plan(rt.idx, od)
+    run = gh.Run(w, rt, gemm_rows=rows)
+    run.plan()
+    mx.moonep_prefetch_weights(run.d, run.ws.buf, run.w_home, run.w_slot)
+    recv = syn.normal_bf16((w.N, w.H), 1.0, 77).cuda()
+    outs = []
+    for _ in range(3):
+        run.y.zero_()
+        mx.moonep_grouped_gemm(run.d, run.ws.buf, recv.view(-1), run.w_home, run.w_slot, run.y)
+        outs.append(run.y.clone())
+    assert mx.moonep_read_status(run.d, run.ws.buf) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    want = olayer.grouped_gemm_rows(gh.host_bits(recv), fp["plan"], gh.host_bits(run.w_home))
+    gh.assert_close(gh.bf16_to_np(outs[2]).reshape(w.N, w.Hp), gh.bits_to_np(want), "repeated gemm")
+    # the input gradient runs the same kernels, claiming from the same counters
+    dy = syn.normal_bf16((w.N, w.Hp), 1.0, 78).cuda()
+    drecv = [torch.zeros(w.N * w.H, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for dr in drecv:
+        mx.moonep_grouped_gemm_dx(run.d, run.ws.buf, dy.view(-1), run.w_home, run.w_slot, dr)
+    assert torch.equal(drecv[0], drecv[1])
+    # weight gradient twice into zeroed gradients: exactly twice one launch (x + x is exact)
+    g1 = [torch.zeros(n, dtype=torch.float32, device="cuda")
+          for n in (w.E * w.H * w.Hp, w.R * w.B * w.H * w.Hp)]
+    g2 = [torch.zeros_like(t) for t in g1]
+    mx.moonep_grouped_gemm_dw(run.d, run.ws.buf, recv.view(-1), dy.view(-1), g1[0], g1[1])
+    for _ in range(2):
+        mx.moonep_grouped_gemm_dw(run.d, run.ws.buf, recv.view(-1), dy.view(-1), g2[0], g2[1])
+    assert mx.moonep_read_status(run.d, run.ws.buf) == 0
+    assert torch.equal(g2[0], 2 * g1[0]) and torch.equal(g2[1], 2 * g1[1])
+    assert bool(g1[0].abs().sum() > 0)
