@@ -836,10 +836,13 @@ __device__ __forceinline__ void tmap_publish(void* map) {
                : "memory");
 }
 
-// Ring depth of the pair kernel (32 KiB stages).  Measured at the pages shape:
-// 4 stages 10.0 ms, 5 stages 9.0 ms, 6 stages 9.2 ms; the sixth stage lets the
-// CTAs run further apart and raises DRAM reads from 29 to 38-41 GB per launch.
-constexpr int kPairStages = 5;
+// Ring depth of the pair kernel (32 KiB stages).  Measured with work items
+// claimed in order, on one box: 6 stages 9.17-9.18 ms at the pages shape and
+// 5.44-5.46 ms at the K3 shape, against 9.23-9.30 and 5.53-5.54 ms with 5.
+// (With a fixed stride per pair the sixth stage had been slower, 9.2 against
+// 9.0 ms: the pairs drifted further apart and panels were evicted before
+// their last reader, 38-41 GB of DRAM reads per launch against 29.)
+constexpr int kPairStages = 6;
 
 template <int STAGES>
 struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns of B
