@@ -18,8 +18,11 @@ Modules:
   force minimum-redundancy search (max-flow feasibility) for tiny inputs.
 
 Parity status: every function above is pinned by tests against facts the
-pages or mathematics fix, except one: *which* copies the planner moves (the
-concrete tie-break) has no external reference, only its invariants do.  That
-choice is "parity unpinned" beyond those invariants.
+pages or mathematics fix.  For the planner the pages fix only invariants;
+*which* copies move follows a tie-break the pages leave open (the plain
+policy's fixed by this build's specification, the largest-first policy's a
+documented reading), and that tie-break is pinned by plans worked by hand
+from the stated rules (tests/golden/hand_plans.json), not by values the
+pages print.
 """
 from . import planner, layer, theory  # noqa: F401
