@@ -19,10 +19,11 @@ Modules:
 
 Parity status: every function above is pinned by tests against facts the
 pages or mathematics fix.  For the planner the pages fix only invariants;
-*which* copies move follows a tie-break the pages leave open (the plain
-policy's fixed by this build's specification, the largest-first policy's a
-documented reading), and that tie-break is pinned by plans worked by hand
-from the stated rules (tests/golden/hand_plans.json), not by values the
-pages print.
+*which* copies move follows a tie-break the pages leave open (for the plain
+policy: smallest-id underloaded and overloaded ranks, the donor's experts in
+descending id, the highest ordinals first; for the largest-first policy: the
+rule stated in planner.constructive_plan), and that tie-break is pinned by
+plans worked by hand from those rules (tests/golden/hand_plans.json), not by
+values the pages print.
 """
 from . import planner, layer, theory  # noqa: F401
