@@ -59,6 +59,13 @@ def _profile128_workload():
     return syn.Workload("profile-sized-128", R=8, E=64, B=8, K=8, S=1024, H=7168, Hp=2048)
 
 
+def _profile_k3_workload():
+    from perfectly_balanced_token_gb300 import synthetic as syn
+    # the K3 shape's per-rank structure (14 experts per rank, K=16, S=1024, H=4096,
+    # H'=1024, ~1.2k rows per group) on 8 ranks instead of 64: about 2 GB on the device
+    return syn.Workload("profile-sized-k3", R=8, E=112, B=14, K=16, S=1024, H=4096, Hp=1024)
+
+
 def _pages():
     from perfectly_balanced_token_gb300 import synthetic as syn
     return syn.PAGES
@@ -70,8 +77,9 @@ def _k3():
 
 
 WORKLOADS = {"pages": _pages, "k3": _k3, "profile": _profile_workload,
-             "profile128": _profile128_workload}
-DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,), "profile128": (1.0,)}
+             "profile128": _profile128_workload, "profile_k3": _profile_k3_workload}
+DEFAULT_SWEEP = {"pages": SWEEP, "k3": (1.0, 10.0), "profile": (1.0,), "profile128": (1.0,),
+                 "profile_k3": (1.0,)}
 
 
 def measured_traffic(kernel: str):
