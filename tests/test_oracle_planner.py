@@ -302,3 +302,41 @@ def test_largest_first_on_the_theorem2_case_reaches_the_bound():
     # rank 0 owns nothing, so any plan gives it >= ceil(E(R-1)/R^2) = 42 experts
     assert p.n_recv[0] >= theory.theorem2_bound(R, E)
     assert max(p.n_recv) <= E // R
+
+
+def test_largest_first_reaches_the_exact_minimax_on_a_seeded_sweep():
+    # [Equilibrage] "La planification en ligne": the online planner is fast and
+    # close to the exact optimum. Against the brute-force minimax (max-flow over
+    # every choice of remote experts) on 240 skewed small instances, the
+    # largest-first policy reaches the optimum every time, while the plain
+    # policy is above it on a large share: a change that made the two policies
+    # pair alike would fail here.
+    above0 = n = 0
+    for (R, E, K, S) in ((2, 6, 2, 12), (3, 6, 2, 8), (4, 8, 4, 8), (4, 12, 2, 8)):
+        for seed in range(60):
+            rt = syn.gumbel_topk_routing(R, S, K, E, alpha=0.5 + (seed % 12) * 0.35, seed=seed)
+            d0 = Dims(R=R, E=E, B=E // R, K=K, S=S)
+            _, T, _ = planner.histogram(rt.idx, d0)
+            m, _ = theory.min_max_redundant(T, R, d0.C, m_max=d0.L)
+            got0 = int(max(planner.build_plan(rt.idx, d0).n_recv))
+            got1 = int(max(planner.build_plan(rt.idx, Dims(R=R, E=E, B=E // R, K=K, S=S,
+                                                           policy=1)).n_recv))
+            assert got1 == m, (R, E, K, S, seed)
+            assert m <= got0 <= d0.L
+            above0 += got0 > m
+            n += 1
+    assert n == 240 and above0 >= n // 4
+
+
+def test_largest_first_is_a_heuristic_not_the_exact_minimax():
+    # one instance (six ranks) where the largest-first pairing needs one more
+    # redundant expert on some rank than the exact minimax: the policy is a
+    # heuristic, as the pages describe their planner
+    R, E, K, S = 6, 12, 2, 6
+    rt = syn.gumbel_topk_routing(R, S, K, E, alpha=0.5, seed=12)
+    d = Dims(R=R, E=E, B=E // R, K=K, S=S, policy=1)
+    _, T, _ = planner.histogram(rt.idx, d)
+    assert T.tolist() == [8, 10, 4, 3, 11, 5, 4, 10, 5, 11, 1, 0]
+    m, _ = theory.min_max_redundant(T, R, d.C, m_max=1)
+    assert m == 1
+    assert planner.build_plan(rt.idx, d).n_recv.tolist() == [1, 1, 1, 0, 1, 2]
