@@ -1396,14 +1396,33 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // has been consumed).
 constexpr int kDwPairStages = 6;
 
+// Permutes the eight 16-byte vectors held in r (four words each) so that slot j
+// holds the vector that was in slot j ^ m (m < 8): three conditional swap stages,
+// one per bit of m, with register indices fixed at compile time.
+__device__ __forceinline__ void xor_vectors8(uint32_t (&r)[32], int m) {
+#pragma unroll
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool s = (m & b) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j & b) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = r[4 * j + w], y = r[4 * (j ^ b) + w];
+        r[4 * j + w] = s ? y : x;
+        r[4 * (j ^ b) + w] = s ? x : y;
+      }
+    }
+  }
+}
+
 template <int STAGES>
 struct GemmCfgDWPair {
   static constexpr int kABytes = kMmaM * kBK * 2;  // 128 H rows x 64 group rows
   static constexpr int kBBytes = 128 * kBK * 2;    // 128 H' columns x 64 group rows
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;            // two 128-lane x 256-column fp32 accumulators
-  static constexpr int kStageOut = 16384;          // 128 rows x 32 fp32, 128-byte swizzled
-  static constexpr int kOutBytes = 2 * kStageOut;
+  static constexpr int kOutBytes = 32768;          // 128 rows x 64 fp32, 256-byte rows, no swizzle
   static constexpr int kNumBars = 2 * STAGES + 5 + 2 * kQueue;
   static constexpr int kBarBytes = kNumBars * 8 + 16 + 4 * kQueue;
   static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
@@ -1615,7 +1634,7 @@ k_ggemm_dw_2sm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           : "memory");
       return r != 0;
     };
-    int acc = 0, chunk = 0;
+    int acc = 0;
     uint32_t acc_phase = 0;
     for (int i = 0;; ++i) {
       int t;
@@ -1643,25 +1662,35 @@ k_ggemm_dw_2sm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0 + (int)crank * kMmaM;
       const uint32_t tbase = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * BN);
       const int rr = qw * 32 + lane;
+      const int m = rr & 7;
+      uint4* row = reinterpret_cast<uint4*>(out_stage + rr * 256);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c, ++chunk) {
-        uint8_t* buf = out_stage + (chunk & 1) * Cfg::kStageOut;
-        if (issuer) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        epi_bar();
-        uint32_t r[32];
-        tmem_ld_x32(tbase + c * 32, r);
+      for (int c = 0; c < BN / 64; ++c) {
+        // this row's 64 columns: 16 vectors of 16 bytes, read from TMEM while the
+        // previous chunk's reduce-add may still be reading the buffer
+        uint32_t lo[32], hi[32];
+        tmem_ld_x32(tbase + c * 64, lo);
+        tmem_ld_x32(tbase + c * 64 + 32, hi);
         tmem_ld_wait();
-        uint4* row = reinterpret_cast<uint4*>(buf + rr * 128);
+        xor_vectors8(lo, m);
+        xor_vectors8(hi, m);
+        if (issuer) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        epi_bar();
+        // the buffer is plain row-major (256-byte rows); each lane writes its
+        // vectors in the order j ^ (row & 7), so the eight lanes of a store phase
+        // hit eight different bank groups
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          row[j ^ (rr & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int j = 0; j < 8; ++j) {
+          row[j ^ m] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+          row[8 + (j ^ m)] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         epi_bar();
         if (issuer) {
           asm volatile(
               "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
               " [%0, {%1, %2}], [%3];" ::"l"((uint64_t)gmap),
-              "r"(n0 + c * 32), "r"(grow), "r"(smem_u32(buf))
+              "r"(n0 + c * 64), "r"(grow), "r"(smem_u32(out_stage))
               : "memory");
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
@@ -1771,7 +1800,8 @@ static bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint
 }
 
 // 2D fp32 tensor [outer][inner] with a box of 128 rows x box_inner, no swizzle
-// (L2 prefetch of a weight-gradient tile).
+// (L2 prefetch of a weight-gradient tile; reduce-add target of the CTA-pair
+// weight-gradient kernel).
 static bool encode_2d_f32_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                                uint32_t box_inner) {
   EncodeTiledFn enc = get_encode();
@@ -1994,10 +2024,16 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void*
   cudaError_t e;
   if (bn == 256 && d.H % (2 * kMmaM) == 0) {
     // 256 x 256 work tiles on CTA pairs: each CTA loads 128 of the 256 H' columns of dY
-    CUtensorMap tdy2;
+    CUtensorMap tdy2, tgh64, tgs64;
     if (!encode_panels_3d(&tdy2, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 2))
       return cudaErrorInvalidValue;
-    e = launch_pair_dw(d, p, tx, tdy2, tgh, tgs, st);
+    // reduce-add targets with a 64-column x 128-row box: 256-byte row segments
+    // stream through L2 and DRAM faster than the 128-byte ones of a 32-column box
+    if (!encode_2d_f32_tile(&tgh64, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64) ||
+        !encode_2d_f32_tile(&tgs64, slots ? g_slot : g_home, (uint64_t)d.Hp,
+                            slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, 64))
+      return cudaErrorInvalidValue;
+    e = launch_pair_dw(d, p, tx, tdy2, tgh64, tgs64, st);
     if (e == cudaSuccess) *launches += 1;
     return e;
   }
