@@ -1133,7 +1133,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
 // 64(h) x 64(row)), B = dY (BN/64 panels of 64(n) x 64(row)).  The reduction
 // runs over the group's rows in 64-row blocks; in the last block the rows past
 // the group's end are zeroed in shared memory before the MMAs.  Accumulators
-// are double buffered in TMEM.  The four epilogue warps stage a 128 x 32 fp32
+// are double buffered in TMEM.  The four epilogue warps stage a 128 x 64 fp32
 // chunk together in shared memory and one thread adds it into G with a TMA
 // reduce-add, so the read-modify-write happens in L2.  Every G element gets
 // one add per launch, always a cold line: for groups long enough to hide it,
@@ -1144,14 +1144,33 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
 // leave too little time for the prefetch and only add DRAM traffic).
 constexpr int kDwPrefetchMinBlocks = 16;
 
+// Permutes the eight 16-byte vectors held in r (four words each) so that slot j
+// holds the vector that was in slot j ^ m (m < 8): three conditional swap stages,
+// one per bit of m, with register indices fixed at compile time.
+__device__ __forceinline__ void xor_vectors8(uint32_t (&r)[32], int m) {
+#pragma unroll
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool s = (m & b) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j & b) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = r[4 * j + w], y = r[4 * (j ^ b) + w];
+        r[4 * j + w] = s ? y : x;
+        r[4 * (j ^ b) + w] = s ? x : y;
+      }
+    }
+  }
+}
+
 template <int BN, int STAGES>
 struct GemmCfgDW {
   static constexpr int kABytes = kMmaM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kStageOut = 16384;           // 128 rows x 32 fp32, 128-byte swizzled
-  static constexpr int kOutBytes = 2 * kStageOut;      // 2 buffers shared by the 4 epilogue warps
+  static constexpr int kOutBytes = 32768;  // 128 rows x 64 fp32, 256-byte rows, no swizzle
   static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
   static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
 };
@@ -1301,10 +1320,11 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
   } else {
     // ---------------- epilogue (warps 2..5): G += accumulator ----------------
-    // Each warp owns 32 rows of the tile.  A 32 x 32 fp32 chunk is drained from
-    // TMEM into one of two swizzled staging buffers and added into G by a TMA
-    // reduce (the read-modify-write happens in L2); a buffer is reused once the
-    // reduce that read it is done.
+    // Each warp owns 32 rows of the tile.  The tile is drained in 128 x 64 fp32
+    // chunks: each row's 64 columns go from TMEM into a plain row-major staging
+    // buffer (256-byte rows) and one thread adds the chunk into G with a TMA
+    // reduce (the read-modify-write happens in L2); the buffer is reused once
+    // the reduce that read it is done.
     const int q = warp & 3;
     const bool issuer = (warp == 2 && lane == 0);
     auto epi_bar = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
@@ -1318,7 +1338,7 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           : "memory");
       return r != 0;
     };
-    int acc = 0, chunk = 0;
+    int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const MTile grp = p.groups[t / per_group];
@@ -1337,25 +1357,32 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int grow = (grp.wsel >= 0 ? grp.wsel : (-1 - grp.wsel)) * d.H + m0;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int rr = q * 32 + lane;
+      const int m = rr & 7;
+      uint4* row = reinterpret_cast<uint4*>(out_stage + rr * 256);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c, ++chunk) {
-        uint8_t* buf = out_stage + (chunk & 1) * Cfg::kStageOut;
-        if (issuer) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        epi_bar();
-        uint32_t r[32];
-        tmem_ld_x32(tbase + c * 32, r);
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t lo[32], hi[32];
+        tmem_ld_x32(tbase + c * 64, lo);
+        tmem_ld_x32(tbase + c * 64 + 32, hi);
         tmem_ld_wait();
-        uint4* row = reinterpret_cast<uint4*>(buf + rr * 128);
+        xor_vectors8(lo, m);
+        xor_vectors8(hi, m);
+        if (issuer) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        epi_bar();
+        // vector order j ^ (row & 7): the eight lanes of a store phase hit eight
+        // different bank groups
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          row[j ^ (rr & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int j = 0; j < 8; ++j) {
+          row[j ^ m] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+          row[8 + (j ^ m)] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         epi_bar();
         if (issuer) {
           asm volatile(
               "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
               " [%0, {%1, %2}], [%3];" ::"l"((uint64_t)gmap),
-              "r"(n0 + c * 32), "r"(grow), "r"(smem_u32(buf))
+              "r"(n0 + c * 64), "r"(grow), "r"(smem_u32(out_stage))
               : "memory");
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
@@ -1395,26 +1422,6 @@ k_ggemm_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // than the stage ring, and a stage is refilled only once its previous load
 // has been consumed).
 constexpr int kDwPairStages = 6;
-
-// Permutes the eight 16-byte vectors held in r (four words each) so that slot j
-// holds the vector that was in slot j ^ m (m < 8): three conditional swap stages,
-// one per bit of m, with register indices fixed at compile time.
-__device__ __forceinline__ void xor_vectors8(uint32_t (&r)[32], int m) {
-#pragma unroll
-  for (int b = 1; b < 8; b <<= 1) {
-    const bool s = (m & b) != 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & b) continue;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t x = r[4 * j + w], y = r[4 * (j ^ b) + w];
-        r[4 * j + w] = s ? y : x;
-        r[4 * (j ^ b) + w] = s ? x : y;
-      }
-    }
-  }
-}
 
 template <int STAGES>
 struct GemmCfgDWPair {
@@ -1786,22 +1793,9 @@ static bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t inner, u
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D fp32 tensor [outer][inner] with a 32 x 128 box, 128-byte swizzle (TMA reduce target).
-static bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t gdim[2] = {inner, outer};
-  cuuint64_t gstride[1] = {inner * 4};
-  cuuint32_t box[2] = {32, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim, gstride, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2D fp32 tensor [outer][inner] with a box of 128 rows x box_inner, no swizzle
-// (L2 prefetch of a weight-gradient tile; reduce-add target of the CTA-pair
-// weight-gradient kernel).
+// (L2 prefetch of a weight-gradient tile; with 64 columns, the reduce-add
+// target of the weight-gradient kernels).
 static bool encode_2d_f32_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                                uint32_t box_inner) {
   EncodeTiledFn enc = get_encode();
@@ -2008,10 +2002,12 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void*
   if (!encode_panels_3d(&tx, recv, (uint64_t)d.H, (uint64_t)d.R * d.C, 2)) return cudaErrorInvalidValue;
   if (!encode_panels_3d(&tdy, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, (uint32_t)pick_bn(d.Hp) / 64))
     return cudaErrorInvalidValue;
-  if (!encode_2d_f32(&tgh, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H)) return cudaErrorInvalidValue;
+  // reduce-add targets with a 64-column x 128-row box: 256-byte row segments
+  // stream through L2 and DRAM faster than the 128-byte ones of a 32-column box
   const bool slots = g_slot != nullptr && d.B > 0;
-  if (!encode_2d_f32(&tgs, slots ? g_slot : g_home, (uint64_t)d.Hp,
-                     slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H))
+  if (!encode_2d_f32_tile(&tgh, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64) ||
+      !encode_2d_f32_tile(&tgs, slots ? g_slot : g_home, (uint64_t)d.Hp,
+                          slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, 64))
     return cudaErrorInvalidValue;
   const int bn = pick_bn(d.Hp);
   // L2 prefetch views of G: one box is a whole 128 x BN work-item tile
@@ -2024,16 +2020,10 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const PlanPtrs& p, const void*
   cudaError_t e;
   if (bn == 256 && d.H % (2 * kMmaM) == 0) {
     // 256 x 256 work tiles on CTA pairs: each CTA loads 128 of the 256 H' columns of dY
-    CUtensorMap tdy2, tgh64, tgs64;
+    CUtensorMap tdy2;
     if (!encode_panels_3d(&tdy2, dy, (uint64_t)d.Hp, (uint64_t)d.R * d.C, 2))
       return cudaErrorInvalidValue;
-    // reduce-add targets with a 64-column x 128-row box: 256-byte row segments
-    // stream through L2 and DRAM faster than the 128-byte ones of a 32-column box
-    if (!encode_2d_f32_tile(&tgh64, g_home, (uint64_t)d.Hp, (uint64_t)d.E * d.H, 64) ||
-        !encode_2d_f32_tile(&tgs64, slots ? g_slot : g_home, (uint64_t)d.Hp,
-                            slots ? (uint64_t)d.R * d.B * d.H : (uint64_t)d.E * d.H, 64))
-      return cudaErrorInvalidValue;
-    e = launch_pair_dw(d, p, tx, tdy2, tgh64, tgs64, st);
+    e = launch_pair_dw(d, p, tx, tdy2, tgh, tgs, st);
     if (e == cudaSuccess) *launches += 1;
     return e;
   }

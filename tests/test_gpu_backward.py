@@ -38,6 +38,9 @@ CASES = [  # H % 128 == 0 for the weight gradient
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=11), 0),
     ("ragged-h384", W("ragged384", R=4, E=12, B=3, K=3, S=400, H=384, Hp=512),
      lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.2, seed=12), 0),
+    # 128-wide weight-gradient column tiles (H' = 384) on the single-CTA kernel
+    ("bn128-h384", W("bn128", R=4, E=8, B=2, K=2, S=300, H=256, Hp=384),
+     lambda w: syn.gumbel_topk_routing(w.R, w.S, w.K, w.E, alpha=1.5, seed=14), 0),
     # every group shorter than one 64-row block: each weight-gradient item's
     # only block runs past the group's end (CTA-pair kernel, H and H' of 256)
     ("groups-under-64-rows", W("short-groups", R=4, E=64, B=16, K=2, S=64, H=256, Hp=256),
