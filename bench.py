@@ -602,49 +602,76 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
-    def pipelined(n):
+    def pipelined(n, detail=None):
         h2d = [Ev() for _ in range(2)]        # inputs of buffer b are on the device
         used = [Ev() for _ in range(2)]       # the step that read buffer b is past combine
         ready = [Ev() for _ in range(2)]      # out[b] holds a finished step
         d2h = [Ev() for _ in range(2)]        # out[b] has been read back
         e0, e1, end = Ev(enable_timing=True), Ev(enable_timing=True), Ev()
+        # where each step's time went: compute and reduce_grad on the compute
+        # stream, each copy on the copy stream
+        t_c = [(Ev(enable_timing=True), Ev(enable_timing=True)) for _ in range(n)]
+        t_in = [(Ev(enable_timing=True), Ev(enable_timing=True)) for _ in range(n)]
+        t_out = [(Ev(enable_timing=True), Ev(enable_timing=True)) for _ in range(n)]
         e0.record(cs)
+        t_in[0][0].record(cs)
         copy_in(0, cs)
+        t_in[0][1].record(cs)
         h2d[0].record(cs)
         for i in range(n):
             b = i % 2
             if i + 1 < n:
                 if i >= 1:
                     cs.wait_event(used[(i + 1) % 2])
+                t_in[i + 1][0].record(cs)
                 copy_in(i + 1, cs)
+                t_in[i + 1][1].record(cs)
                 h2d[(i + 1) % 2].record(cs)
             st.wait_event(h2d[b])
             if i >= 2:
                 st.wait_event(d2h[b])
+            t_c[i][0].record(st)
             compute(i)
             used[b].record(st)
             ready[b].record(st)
             mx.moonep_reduce_grad(d, ws.buf, g_home, g_slot, st)
+            t_c[i][1].record(st)
             cs.wait_event(ready[b])
+            t_out[i][0].record(cs)
             copy_out(i, cs)
+            t_out[i][1].record(cs)
             d2h[b].record(cs)
         end.record(st)
         cs.wait_event(end)
         e1.record(cs)
         torch.cuda.synchronize()
+        if detail is not None:
+            span = lambda p: p[0].elapsed_time(p[1])
+            med = lambda xs: float(np.median(xs))
+            detail.update({
+                "compute_ms_median": med([span(p) for p in t_c]),
+                "copy_in_ms_median": med([span(p) for p in t_in]),
+                "copy_out_ms_median": med([span(p) for p in t_out]),
+                # compute-stream idle time between one step's end and the next's start
+                "idle_between_steps_ms": [round(t_c[i - 1][1].elapsed_time(t_c[i][0]), 3)
+                                          for i in range(1, n)],
+                "first_step_start_ms": e0.elapsed_time(t_c[0][0]),
+            })
         return e0.elapsed_time(e1)
 
     serial(2)
     pipelined(2)
     ms_serial = reduce_max(serial(steps), world, dev)
-    ms = reduce_max(pipelined(steps), world, dev)
+    detail = {}
+    ms = reduce_max(pipelined(steps, detail), world, dev)
     h2d_bytes = x_h.numel() * 2 + idx_h[0].numel() * 4 + g_h[0].numel() * 4
     return {"value": N * steps * world / (ms / 1e3), "unit": UNIT, "steps": steps,
             "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(out_h[0].numel() * 2),
             "schedule": "copies on a second stream, double-buffered, overlapping the previous "
                         "and next steps' compute",
             "serial_value": N * steps * world / (ms_serial / 1e3),
-            "serial_schedule": "copy-in, step, copy-out on one stream"}
+            "serial_schedule": "copy-in, step, copy-out on one stream",
+            "pipelined_detail": detail}
 
 
 # ----------------------------------------------------------------------------
