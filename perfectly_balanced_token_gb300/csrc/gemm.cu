@@ -850,11 +850,13 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
   static constexpr int kBBytes = 128 * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;  // two 128-lane x 256-column fp32 accumulators
+  // output staging: per epilogue warp two 32-row x 64-column bf16 buffers
+  // (128-byte rows, 128-byte swizzle), the sources of its TMA stores
+  static constexpr int kOutWarpBytes = 2 * 4096;
+  static constexpr int kOutBytes = 4 * kOutWarpBytes;
   static constexpr int kNumBars = 2 * STAGES + 5 + 2 * kQueue;
   static constexpr int kBarBytes = kNumBars * 8 + 16 + 4 * kQueue;
-  // 32 KiB of slack past the barriers: one CTA per SM either way, and no
-  // operand read of the last stage can leave this CTA's allocation
-  static constexpr int kSmem = STAGES * kStageBytes + 1024 + kBarBytes + 32768;
+  static constexpr int kSmem = STAGES * kStageBytes + kOutBytes + 1024 + kBarBytes;
 };
 
 // 256 x 256 work tiles on a CTA pair with the pair form of the MMA
@@ -884,13 +886,14 @@ struct GemmCfgPair {  // per CTA: its 128 rows of A and 128 of the 256 columns o
 template <int STAGES, bool BKM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
-            const __grid_constant__ CUtensorMap tm_ws, Dims d, GemmShape sh, PlanPtrs p,
-            uint16_t* __restrict__ y) {
+            const __grid_constant__ CUtensorMap tm_ws, const __grid_constant__ CUtensorMap tm_y,
+            Dims d, GemmShape sh, PlanPtrs p, uint16_t* __restrict__ y) {
   using Cfg = GemmCfgPair<STAGES>;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * Cfg::kStageBytes);
+  uint8_t* out_stage = smem + STAGES * Cfg::kStageBytes;  // 1024-aligned
+  uint64_t* bars = (uint64_t*)(out_stage + Cfg::kOutBytes);
   uint32_t* tmem_slot = (uint32_t*)(bars + Cfg::kNumBars);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -931,6 +934,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_wh);
     prefetch_tmap(&tm_ws);
+    prefetch_tmap(&tm_y);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -1058,7 +1062,7 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   } else {
     // ---------------- epilogue (warps 2..5, both CTAs) ----------------
     const int qw = warp & 3;
-    int acc = 0;
+    int acc = 0, nstore = 0;
     uint32_t acc_phase = 0;
     for (int i = 0;; ++i) {
       int t;
@@ -1081,25 +1085,64 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
         break;
       }
       tc_fence_after();
-      const int row = (int)crank * kMmaM + qw * 32 + lane;
-      const bool valid = row < mt.rows;
-      uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
+      const int wrow0 = (int)crank * kMmaM + qw * 32;  // this warp's first row of the tile
       const uint32_t tbase = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * BN);
+      if (wrow0 + 32 <= mt.rows) {
+        // all 32 rows inside the group: bf16 rows staged in shared memory
+        // (128-byte swizzle, so the lanes of a store phase hit distinct bank
+        // groups) and written by one TMA store per 64 columns
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_x32(tbase + c * 32, r);
-        tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+        for (int c = 0; c < BN / 64; ++c, ++nstore) {
+          uint32_t lo[32], hi[32];
+          tmem_ld_x32(tbase + c * 64, lo);
+          tmem_ld_x32(tbase + c * 64 + 32, hi);
+          tmem_ld_wait();
+          uint8_t* buf = out_stage + qw * Cfg::kOutWarpBytes + (nstore & 1) * 4096;
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+          uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 128);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
-            o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
-            o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
-            o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
-            dst[v] = o;
+            rowp[v ^ (lane & 7)] =
+                make_uint4(pack_bf16x2(lo[8 * v + 0], lo[8 * v + 1]), pack_bf16x2(lo[8 * v + 2], lo[8 * v + 3]),
+                           pack_bf16x2(lo[8 * v + 4], lo[8 * v + 5]), pack_bf16x2(lo[8 * v + 6], lo[8 * v + 7]));
+            rowp[(4 + v) ^ (lane & 7)] =
+                make_uint4(pack_bf16x2(hi[8 * v + 0], hi[8 * v + 1]), pack_bf16x2(hi[8 * v + 2], hi[8 * v + 3]),
+                           pack_bf16x2(hi[8 * v + 4], hi[8 * v + 5]), pack_bf16x2(hi[8 * v + 6], hi[8 * v + 7]));
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                    (uint64_t)&tm_y),
+                "r"(n0 + c * 64), "r"(mt.row0 + wrow0), "r"(smem_u32(buf))
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
+      } else {
+        // rows past the group's end belong to the next group: each lane
+        // stores its own row if it is inside the group
+        const int row = wrow0 + lane;
+        const bool valid = row < mt.rows;
+        uint16_t* yrow = y + (size_t)(mt.row0 + row) * sh.N + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tbase + c * 32, r);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+              o.y = pack_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+              o.z = pack_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+              o.w = pack_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+              dst[v] = o;
+            }
           }
         }
       }
@@ -1108,6 +1151,8 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       if (lane == 0) mbar_arrive_remote(pair_map(tempty(acc), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this warp's stores
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1862,6 +1907,8 @@ static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs&
                                     const CUtensorMap& a, const CUtensorMap& wh,
                                     const CUtensorMap& ws, uint16_t* y, cudaStream_t st) {
   using Cfg = GemmCfgPair<kPairStages>;
+  CUtensorMap ty;  // the output as TMA store target, 32-row boxes of 64 columns
+  if (!encode_2d(&ty, y, (uint64_t)sh.N, (uint64_t)d.R * d.C, 32)) return cudaErrorInvalidValue;
   static int grid = 0;
   if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(k_ggemm_2sm<kPairStages, BKM>,
@@ -1877,7 +1924,7 @@ static cudaError_t launch_pair_gemm(const Dims& d, GemmShape sh, const PlanPtrs&
     grid = 2 * std::max(1, ncl);
   }
   if (grid > kMaxGemmCtas) return cudaErrorInvalidConfiguration;  // tensor-map scratch per CTA
-  k_ggemm_2sm<kPairStages, BKM><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, d, sh, p, y);
+  k_ggemm_2sm<kPairStages, BKM><<<grid, kGemmThreads, Cfg::kSmem, st>>>(a, wh, ws, ty, d, sh, p, y);
   return cudaGetLastError();
 }
 
