@@ -229,11 +229,12 @@ k_combine(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restri
 // backward of combine: for out[t] = sum_k g[t,k] Y[dst(t,k)],
 //   dY[dst(t,k)] = bf16(g[t,k] * dout[t])   and   dg[t,k] = <Y[dst(t,k)], dout[t]>
 // (fp32 products and sums).  One CTA per token; each thread keeps its slice of
-// the dout row in registers; the K dot products are block reductions.
+// the dout row in registers; the copies are taken KC at a time, their Y loads
+// all issued before the first is used; the K dot products are block reductions.
 // ---------------------------------------------------------------------------
 constexpr int kBwdMaxK = 128;
 
-template <int VPT>
+template <int VPT, int KC>
 __global__ void __launch_bounds__(kRowThreads)
 k_combine_bwd(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __restrict__ gates,
               const uint4* __restrict__ dout, uint4* __restrict__ dy, float* __restrict__ dgates) {
@@ -263,31 +264,55 @@ k_combine_bwd(Dims d, PlanPtrs p, const uint4* __restrict__ y, const float* __re
     }
     const int32_t* dt = p.dst + (size_t)t * d.K;
     const float* gt = gates + (size_t)t * d.K;
-    for (int k = 0; k < d.K; ++k) {
-      const size_t row = (size_t)__ldg(dt + k);
-      const float g = __ldg(gt + k);
-      float dot = 0.f;
+    for (int k0 = 0; k0 < d.K; k0 += KC) {
+      size_t row[KC];
+      float g[KC];
+      uint4 v[KC][VPT];
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int a = threadIdx.x + i * kRowThreads;
-        if (a < hv) {
-          const uint4 v = __ldcs(y + row * hv + a);
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-          uint4 w;
-          __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+      for (int k = 0; k < KC; ++k) {
+        row[k] = k0 + k < d.K ? (size_t)__ldg(dt + k0 + k) : 0;
+        g[k] = k0 + k < d.K ? __ldg(gt + k0 + k) : 0.f;
+      }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(h[j]);
-            dot = fmaf(f.x, o[i][2 * j], dot);
-            dot = fmaf(f.y, o[i][2 * j + 1], dot);
-            hw[j] = __floats2bfloat162_rn(g * o[i][2 * j], g * o[i][2 * j + 1]);
+      for (int k = 0; k < KC; ++k)
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int a = threadIdx.x + i * kRowThreads;
+          if (k0 + k < d.K && a < hv) v[k][i] = __ldcs(y + row[k] * hv + a);
+        }
+      float dot[KC];
+#pragma unroll
+      for (int k = 0; k < KC; ++k) {
+        dot[k] = 0.f;
+        if (k0 + k < d.K) {
+#pragma unroll
+          for (int i = 0; i < VPT; ++i) {
+            const int a = threadIdx.x + i * kRowThreads;
+            if (a < hv) {
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[k][i]);
+              uint4 w;
+              __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(h[j]);
+                dot[k] = fmaf(f.x, o[i][2 * j], dot[k]);
+                dot[k] = fmaf(f.y, o[i][2 * j + 1], dot[k]);
+                hw[j] = __floats2bfloat162_rn(g[k] * o[i][2 * j], g[k] * o[i][2 * j + 1]);
+              }
+              __stcs(dy + row[k] * hv + a, w);
+            }
           }
-          __stcs(dy + row * hv + a, w);
         }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      if (lane == 0) part[warp][k] = dot;
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int k = 0; k < KC; ++k) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], off);
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+          if (k0 + k < d.K) part[warp][k0 + k] = dot[k];
+      }
     }
     __syncthreads();
     for (int k = threadIdx.x; k < d.K; k += kRowThreads) {
@@ -497,10 +522,11 @@ cudaError_t launch_combine_backward(const Dims& d, const PlanPtrs& p, const void
   const uint4 *ys = (const uint4*)y, *os = (const uint4*)dout;
   uint4* dys = (uint4*)dy;
   if (d.K > kBwdMaxK) return cudaErrorInvalidValue;
-  if (vpt <= 1) k_combine_bwd<1><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
-  else if (vpt <= 2) k_combine_bwd<2><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
-  else if (vpt <= 4) k_combine_bwd<4><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
-  else if (vpt <= 8) k_combine_bwd<8><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  // KC x VPT row vectors in flight per thread: 8 for every row width
+  if (vpt <= 1) k_combine_bwd<1, 8><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 2) k_combine_bwd<2, 4><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 4) k_combine_bwd<4, 2><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
+  else if (vpt <= 8) k_combine_bwd<8, 1><<<grid, kRowThreads, 0, st>>>(d, p, ys, gates, os, dys, dgates);
   else return cudaErrorInvalidValue;
   *launches += 1;
   return cudaGetLastError();
