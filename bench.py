@@ -473,6 +473,17 @@ def run_ours(args):
         rooflines[k] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                         "frac": gbs / hbm_peak, "bytes_per_launch": b, "ms_per_launch": ms}
     rooflines["plan"] = {"bound": "latency", "us_per_launch": float(seg[:, 0].mean()) * 1e3}
+    if training is not None:
+        # the backward's streaming kernels against the same HBM peak
+        tb = {"combine_backward": (2 * N + w.R * w.S) * w.Hp * 2 + N * 12,
+              "dispatch_backward": (N + w.R * w.S) * w.H * 2 + N * 4}
+        training["rooflines"] = {}
+        for k, b in tb.items():
+            ms = training["breakdown_ms"][k]
+            gbs = b / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+            training["rooflines"][k] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                        "unit": "GB/s", "frac": gbs / hbm_peak,
+                                        "bytes_per_launch": b, "ms_per_launch": ms}
 
     result = {
         "metric": METRIC, "value": N * args.steps * world / (total_ms / 1e3), "unit": UNIT,
