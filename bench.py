@@ -765,11 +765,55 @@ def blas_threads() -> int:
     return int(os.environ.get("OPENBLAS_NUM_THREADS", HOST_THREADS))
 
 
+class _SlotRows(dict):
+    """The occupied slots' gradient rows keyed by (rank, slot); assigning a
+    scalar fills the row in place, as it does for a slice of one array."""
+
+    def __setitem__(self, key, value):
+        dict.__getitem__(self, key)[...] = value
+
+
+def oracle_reduce_sample(seed: int = 0):
+    """The oracle's reduce_grad timed on its own on the occupied slots of the
+    pages-shaped maxvio-1 plan: every expert holding a slot and every occupied
+    slot, fp32 N(0,1) rows (the experts renumbered so only they are held)."""
+    from types import SimpleNamespace
+
+    from oracle import layer as olayer
+    from oracle import planner as oplanner
+    from perfectly_balanced_token_gb300 import synthetic as syn
+
+    w = syn.PAGES
+    od = oplanner.Dims(R=w.R, E=w.E, B=w.B, K=w.K, S=w.S, H=w.H, Hp=w.Hp)
+    plan = oplanner.build_plan(syn.routing_for(w, 1.0, seed=seed).idx, od)
+    occ = [(u, j, int(plan.slot_expert[u, j])) for u in range(w.R) for j in range(w.B)
+           if plan.slot_expert[u, j] >= 0]
+    experts = sorted({e for _, _, e in occ})
+    local = {e: i for i, e in enumerate(experts)}
+    rng = np.random.default_rng(seed)
+    g_home = rng.standard_normal((len(experts), w.H, w.Hp), dtype=np.float32)
+    slots = _SlotRows({(u, j): rng.standard_normal((w.H, w.Hp), dtype=np.float32)
+                       for u, j, _ in occ})
+    se = np.full((w.R, w.B), -1, dtype=np.int64)
+    for u, j, e in occ:
+        se[u, j] = local[e]
+    view = SimpleNamespace(dims=SimpleNamespace(E=len(experts), R=w.R, B=w.B), slot_expert=se)
+    t0 = time.perf_counter()
+    olayer.reduce_grad(g_home, slots, view, experts=range(len(experts)))
+    sec = time.perf_counter() - t0
+    nbytes = (len(experts) + len(occ)) * w.H * w.Hp * 4 * 2
+    return {"ms": sec * 1e3, "experts": len(experts), "occupied_slots": len(occ),
+            "bytes": nbytes, "gbs": nbytes / sec / 1e9,
+            "sample": "oracle reduce_grad of the maxvio-1 plan's occupied slots into their "
+                      "home experts (home rows read and written, slots read and zeroed)"}
+
+
 def cpu_baseline(budget_s: float):
     v, desc, _ = OracleSample().run(budget_s)
     return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": desc, "host_cores": os.cpu_count(),
-            "threads_note": "OMP_NUM_THREADS / OPENBLAS_NUM_THREADS set to the host core count"}
+            "threads_note": "OMP_NUM_THREADS / OPENBLAS_NUM_THREADS set to the host core count",
+            "reduce_grad": oracle_reduce_sample()}
 
 
 def run_reference(args):
