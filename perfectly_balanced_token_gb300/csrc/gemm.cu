@@ -343,8 +343,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 
 // ---- work items of a CTA pair, claimed in order -------------------------------
 // The pair's leader claims work items one at a time from a counter in global
-// memory and hands each to every role of both CTAs through a ring of kQueue
-// shared-memory slots; -1 ends the sequence.  Claiming in order keeps the
+// memory, one item ahead of the one it hands out (so the atomic's round trip
+// overlaps an item's loads), and hands each to every role of both CTAs
+// through a ring of kQueue shared-memory slots; -1 ends the sequence.  Claiming in order keeps the
 // items that run at the same time contiguous in the work order (they share
 // operand rows and weight panels in L2) and lets a pair that runs a little
 // faster take more items: with a fixed stride the pairs drifted apart by the
@@ -498,10 +499,13 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // items are claimed one ahead: the next claim travels while this item's
+      // loads are issued
+      int next = atomicAdd(p.sched + 4, 1);
       for (int i = 0; ok; ++i) {
-        int t = atomicAdd(p.sched + 4, 1);  // claim the next item
-        if (t >= total) t = -1;
+        const int t = next >= total ? -1 : next;
         if (!queue_push(q, i, t, abort_flag, false)) { ok = false; break; }
+        if (t >= 0) next = atomicAdd(p.sched + 4, 1);
         if (t < 0) break;
         const MTile mt = p.mtiles[t / NT];
         const int n0 = (t % NT) * BN;
@@ -959,12 +963,15 @@ k_ggemm_2sm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       int stage = 0, issued = 0, slot = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // the leader claims one item ahead: the claim of the next item travels
+      // while this one's loads are issued
+      int next = leader ? atomicAdd(p.sched, 1) : 0;
       for (int i = 0; ok; ++i) {
         int t;
-        if (leader) {  // claim the next item for the pair
-          t = atomicAdd(p.sched, 1);
-          if (t >= total) t = -1;
+        if (leader) {  // hand the claimed item to the pair, claim the following one
+          t = next >= total ? -1 : next;
           if (!queue_push(q, i, t, abort_flag)) { ok = false; break; }
+          if (t >= 0) next = atomicAdd(p.sched, 1);
         } else if (!queue_take(q, i, false, true, t, abort_flag)) {
           ok = false;
           break;
@@ -1570,12 +1577,15 @@ k_ggemm_dw_2sm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       int stage = 0, issued = 0, slot = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // the leader claims one item ahead: the claim of the next item travels
+      // while this one's loads are issued
+      int next = leader ? atomicAdd(p.sched + 2, 1) : 0;
       for (int i = 0; ok; ++i) {
         int t;
-        if (leader) {  // claim the next item for the pair
-          t = atomicAdd(p.sched + 2, 1);
-          if (t >= total) t = -1;
+        if (leader) {  // hand the claimed item to the pair, claim the following one
+          t = next >= total ? -1 : next;
           if (!queue_push(q, i, t, abort_flag)) { ok = false; break; }
+          if (t >= 0) next = atomicAdd(p.sched + 2, 1);
         } else if (!queue_take(q, i, false, true, t, abort_flag)) {
           ok = false;
           break;
