@@ -7,29 +7,28 @@
 // multiplied by W_home[g] (g < E) or by slot (u, g-E).
 //
 // Design (sm_103a):
-//  * two variants, with work tiles of 128 rows (k_ggemm_m128) and of 256 rows
-//    (k_ggemm_m256); every plan picks one with the cost model of
-//    gemm_cost.cuh and records it in the workspace.  Both are launched; the
-//    one not chosen returns before touching anything.
-//  * persistent CTAs, one per SM; the work list is the planner's list of
-//    work tiles of up to 128 or 256 rows of one group (device memory), times H'/BN
-//    column tiles.  Column tiles of one row tile are adjacent in the order, so
-//    concurrently running CTAs share the A rows and all tiles of one group
-//    share the expert's weights in L2.
-//  * a work tile is two 128-row halves that share every B stage: two
-//    128 x BN fp32 accumulators in TMEM (2*BN columns).  Per 64-deep K block a
-//    stage holds 2 A boxes and one B panel, so each byte of B fetched from L2
-//    feeds twice the MMA work of a single 128-row tile.  A tile whose group
-//    ends within its first half issues only the first half's MMAs.
-//  * warp 0: TMA producer (A boxes 64x128 K-major; B as BN/64 panels of 64x64
-//    N-major fetched by one 3D box; all 128-byte swizzled) into a
-//    STAGES-deep shared-memory ring;
-//    warp 1: TMEM allocation and the single-thread tcgen05.mma issuer
-//    (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM);
-//    warps 2..5: epilogue, tcgen05.ld of an accumulator, bf16 rounding
-//    (nearest even), masked row stores.  Each accumulator is released as soon
-//    as it is drained, so the next tile's first-half MMAs overlap the drain of
-//    the second half.
+//  * forward and input gradient: work tiles of 128 rows (k_ggemm_m128, one
+//    CTA) or of 256 rows (k_ggemm_2sm on a CTA pair with the pair form of the
+//    MMA when N is a multiple of 256, else k_ggemm_m256 on one CTA as two
+//    128-row halves); every plan picks the height with the cost model of
+//    gemm_cost.cuh and records it in the workspace.  Both heights are
+//    launched; the one not chosen returns before touching anything.
+//  * weight gradient: (group, 256 H rows, 256 H' columns) items on CTA pairs
+//    (k_ggemm_dw_2sm) when H and H' are multiples of 256, else 128-row items
+//    on one CTA (k_ggemm_dw); the accumulator is added into the fp32 gradient
+//    with TMA reduce-adds.
+//  * persistent CTAs (or CTA pairs), one per SM; the work list is the
+//    planner's list of work tiles (or groups) of one group, times the column
+//    tiles, claimed in order from a counter one item ahead.  Column tiles of
+//    one row tile are adjacent in the order, so the items running together
+//    share A rows and an expert's weights in L2.
+//  * roles: warp 0 the TMA producer into a STAGES-deep shared-memory ring
+//    (128-byte swizzled boxes); warp 1 TMEM allocation and the single-thread
+//    tcgen05.mma issuer (bf16 x bf16 -> fp32 in TMEM, double-buffered
+//    accumulators); warps 2..5 the epilogue: tcgen05.ld, bf16 rounding
+//    (nearest even) and stores (TMA stores of 32-row slices in the pair
+//    kernel, masked row stores where rows run past a group's end and in the
+//    single-CTA kernels).
 //  * every mbarrier wait is bounded by the global timer; on expiry the kernel
 //    records MOONEP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and
 //    returns.
@@ -634,7 +633,12 @@ k_ggemm_m128(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
   }
 }
 
-// Two 128-row halves per work item sharing each B stage.
+// 256-row work tiles on one CTA (N not a multiple of 256): two 128-row halves
+// share every B stage, with two 128 x BN fp32 accumulators in TMEM (2*BN
+// columns), so each byte of B fetched from L2 feeds twice the MMA work of a
+// 128-row tile.  A tile whose group ends within its first half issues only the
+// first half's MMAs.  Each accumulator is released as soon as it is drained,
+// so the next tile's first-half MMAs overlap the drain of the second half.
 template <int BN, int STAGES, bool BKM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_ggemm_m256(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_wh,
