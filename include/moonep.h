@@ -298,9 +298,8 @@ int moonep_selftest_bounded_wait(int32_t* dev_status, uint32_t limit_us, int32_t
  *
  * There is no counterpart on the pages: this is an operational variant.  Some
  * callers cannot call cudaMalloc at planning time -- for example code running
- * inside a pre-sized memory pool or arena that must not grow, a caching
- * allocator that forbids new allocations after warm-up, or a runtime that
- * plans between captured graph segments.  This entry point computes exactly
+ * inside a pre-sized memory pool or arena that must not grow, or a caching
+ * allocator that forbids new allocations after warm-up.  This entry point computes exactly
  * what moonep_plan computes (same workspace layout, same output tables, bit
  * for bit) but keeps the planner's internal scratch -- the per-chunk expert
  * counts, the per-expert migrated ranges and their row bases, and the per-rank
@@ -314,8 +313,7 @@ int moonep_selftest_bounded_wait(int32_t* dev_status, uint32_t limit_us, int32_t
  * table (its internal scratch regions, `counts` among them, are left
  * untouched).  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current and keeps it for
- * the life of the process; make that first call before any stream capture.
- * A cudaDeviceReset of that device invalidates the kept address, so this
+ * the life of the process.  A cudaDeviceReset of that device invalidates the kept address, so this
  * entry point must not be called on a device after it has been reset.
  * Every call shares the one array, which keeps the last call's contents:
  * calls whose kernels overlap on the GPU (two streams, or two host threads)
