@@ -558,7 +558,7 @@ def time_send_once(mx, torch, d, ws, w, sweep, idx, x, gates, recv, flush, warmu
 
 
 def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_slot, dev, st,
-            world):
+            world, verify_steps=0):
     """Same step, but x / routing / gates start in pinned host memory and the
     combined output is read back to pinned host memory every step.
 
@@ -567,13 +567,22 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
     (the reported value) issues the copies on two more streams (inputs, and
     outputs) into double buffers, so step i+1's inputs travel and step i-1's
     output returns while step i computes, as a data loader feeding this layer
-    would."""
+    would.
+
+    With verify_steps > 0 nothing is timed: that many steps go through the
+    pipelined schedule with inputs that change from step to step (three token
+    matrices and the routings in turn, so no two steps that share a buffer
+    have the same inputs), every step's read-back is kept, and the result
+    counts the steps whose output differs from the same step run alone on one
+    stream."""
     N = w.N
-    x_h = syn.normal_bf16((w.R, w.S, w.H), 1.0, 1, "cpu").pin_memory()
+    nx = 3 if verify_steps else 1
+    x_h = [syn.normal_bf16((w.R, w.S, w.H), 1.0, 1 + i, "cpu").pin_memory() for i in range(nx)]
     idx_h = [torch.from_numpy(r.idx).pin_memory() for r in routings]
     g_h = [torch.from_numpy(r.gates).pin_memory() for r in routings]
     out_h = [torch.empty(w.R * w.S * w.Hp, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    x_d = [torch.empty_like(x_h, device=dev) for _ in range(2)]
+    x_d = [torch.empty_like(x_h[0], device=dev) for _ in range(2)]
+    kept = None  # per-step copies of the read-backs (verification only)
     idx_d = [torch.empty_like(idx_h[0], device=dev) for _ in range(2)]
     g_d = [torch.empty_like(g_h[0], device=dev) for _ in range(2)]
     out = [torch.empty(w.R * w.S * w.Hp, dtype=torch.bfloat16, device=dev) for _ in range(2)]
@@ -589,7 +598,7 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
     def copy_in(i, stream):
         b, j = i % 2, i % len(routings)
         with torch.cuda.stream(stream):
-            x_d[b].copy_(x_h, non_blocking=True)
+            x_d[b].copy_(x_h[i % nx], non_blocking=True)
             idx_d[b].copy_(idx_h[j], non_blocking=True)
             g_d[b].copy_(g_h[j], non_blocking=True)
 
@@ -604,6 +613,8 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
     def copy_out(i, stream):
         with torch.cuda.stream(stream):
             out_h[i % 2].copy_(out[i % 2], non_blocking=True)
+            if kept is not None:
+                kept[i].copy_(out[i % 2], non_blocking=True)
 
     def serial(n):
         e0, e1 = Ev(enable_timing=True), Ev(enable_timing=True)
@@ -675,6 +686,17 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
             })
         return e0.elapsed_time(e1)
 
+    if verify_steps:
+        kept = [torch.empty_like(out_h[0]).pin_memory() for _ in range(verify_steps)]
+        pipelined(verify_steps)
+        bad = 0
+        for i in range(verify_steps):
+            copy_in(i, st)
+            compute(i)
+            torch.cuda.synchronize()
+            bad += int(not torch.equal(out[i % 2].cpu(), kept[i]))
+        return {"steps": verify_steps, "mismatches": bad}
+
     serial(2)
     pipelined(2)
     # each schedule is timed seven times and the median run reported: the host
@@ -689,7 +711,7 @@ def run_e2e(args, mx, syn, torch, d, w, routings, ws, w_home, w_slot, g_home, g_
         runs.append((reduce_max(pipelined(steps, det), world, dev), det))
     ms_serial = sorted(serial_ms)[reps // 2]
     ms, detail = sorted(runs, key=lambda r: r[0])[reps // 2]
-    h2d_bytes = x_h.numel() * 2 + idx_h[0].numel() * 4 + g_h[0].numel() * 4
+    h2d_bytes = x_h[0].numel() * 2 + idx_h[0].numel() * 4 + g_h[0].numel() * 4
     return {"value": N * steps * world / (ms / 1e3), "unit": UNIT, "steps": steps,
             "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(out_h[0].numel() * 2),
             "schedule": "copies in and out on two more streams, double-buffered, overlapping the "
