@@ -139,6 +139,22 @@ int moonep_plan_workspace_bytes(const moonep_dims* dims, size_t* bytes);
 /* Offsets of the workspace tables, so callers can view them (host only). */
 int moonep_get_plan_layout(const moonep_dims* dims, moonep_plan_layout* out);
 
+/* Device pointers to the plan's main tables inside a plan workspace: the
+ * buffer views and cu_seqlens the pages' dispatch hands back ("Moonshot AI 开源
+ * MoonEP", contract paragraph).  Host only: computed from the layout, no GPU
+ * work and no synchronisation.  plan_ws is the device workspace (16-byte
+ * aligned) that moonep_plan fills; the pointers stay valid as long as it does
+ * and the tables hold the last plan written into it.  Returns MOONEP_ERR_ARG
+ * for a NULL plan_ws or out, MOONEP_ERR_ALIGN for a misaligned plan_ws. */
+typedef struct moonep_plan_view {
+  const int32_t* cu_seqlens;  /* [R][E+B+1] group boundaries of each rank's buffer */
+  const int32_t* dst;         /* [R][S][K] destination row u*C + row of each copy  */
+  const int32_t* inverse;     /* [R*C] flat copy id (r*S+s)*K+k of each row         */
+  const int32_t* slot_expert; /* [R][B] expert held by slot (u,j), -1 if empty      */
+  const int32_t* status;      /* the sticky device status word                      */
+} moonep_plan_view;
+int moonep_plan_views(const moonep_dims* dims, const void* plan_ws, moonep_plan_view* out);
+
 /* Plan one layer from the router's top-K output.
  *
  * Defines: the histogram, and the constructive balancing plan of Theorem 1

@@ -6,6 +6,7 @@ from ._lib import (  # noqa: F401
     moonep_dispatch, moonep_dispatch_backward, moonep_grouped_gemm_dw, moonep_grouped_gemm_dx,
     moonep_dispatch_send_once,
     moonep_get_plan_layout, moonep_grouped_gemm, moonep_launch_count, moonep_plan,
-    moonep_plan_noalloc, moonep_plan_workspace_bytes, moonep_prefetch_weights, moonep_read_status,
+    moonep_plan_noalloc, moonep_plan_views, moonep_plan_workspace_bytes, moonep_prefetch_weights,
+    moonep_read_status,
     moonep_reduce_grad, moonep_selftest_bounded_wait, status_string,
 )

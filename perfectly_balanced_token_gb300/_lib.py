@@ -59,6 +59,11 @@ class moonep_plan_layout(ctypes.Structure):
         ("groups", ctypes.c_size_t)]
 
 
+class moonep_plan_view(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("cu_seqlens", "dst", "inverse", "slot_expert",
+                                                 "status")]
+
+
 _lib = None
 
 
@@ -75,6 +80,7 @@ def library() -> ctypes.CDLL:
     sig = {
         "moonep_plan_workspace_bytes": [D, ctypes.POINTER(ctypes.c_size_t)],
         "moonep_get_plan_layout": [D, ctypes.POINTER(moonep_plan_layout)],
+        "moonep_plan_views": [D, P, ctypes.POINTER(moonep_plan_view)],
         "moonep_plan": [D, P, P, P],
         "moonep_prefetch_weights": [D, P, P, P, P],
         "moonep_dispatch": [D, P, P, P, P],
@@ -157,6 +163,17 @@ def moonep_get_plan_layout(d: moonep_dims) -> moonep_plan_layout:
     _check(library().moonep_get_plan_layout(ctypes.byref(d), ctypes.byref(out)),
            "moonep_get_plan_layout")
     return out
+
+
+def moonep_plan_views(d: moonep_dims, plan_ws) -> dict:
+    """Device addresses of cu_seqlens, dst, inverse, slot_expert and the status
+    word inside plan_ws (a CUDA uint8 tensor of the workspace size, or its
+    device address as an int); host only."""
+    addr = plan_ws if isinstance(plan_ws, int) else _ws(d, plan_ws)
+    out = moonep_plan_view()
+    _check(library().moonep_plan_views(ctypes.byref(d), addr, ctypes.byref(out)),
+           "moonep_plan_views")
+    return {n: getattr(out, n) for n, _ in moonep_plan_view._fields_}
 
 
 def _ws(d, ws):

@@ -195,6 +195,22 @@ int moonep_get_plan_layout(const moonep_dims* dims, moonep_plan_layout* out) {
   return MOONEP_OK;
 }
 
+int moonep_plan_views(const moonep_dims* dims, const void* plan_ws, moonep_plan_view* out) {
+  Dims d;
+  const int rc = check_dims(dims, &d);
+  if (rc != MOONEP_OK) return rc;
+  if (plan_ws == nullptr || out == nullptr) return MOONEP_ERR_ARG;
+  if (!aligned16(plan_ws)) return MOONEP_ERR_ALIGN;
+  const moonep_plan_layout L = make_layout(d).pub;
+  const uint8_t* b = static_cast<const uint8_t*>(plan_ws);
+  out->cu_seqlens = reinterpret_cast<const int32_t*>(b + L.cu_seqlens);
+  out->dst = reinterpret_cast<const int32_t*>(b + L.dst);
+  out->inverse = reinterpret_cast<const int32_t*>(b + L.inverse);
+  out->slot_expert = reinterpret_cast<const int32_t*>(b + L.slot_expert);
+  out->status = reinterpret_cast<const int32_t*>(b + L.status);
+  return MOONEP_OK;
+}
+
 int moonep_plan(const moonep_dims* dims, const int32_t* topk_idx, void* plan_ws, void* stream) {
   MOONEP_PROLOGUE(dims, plan_ws);
   MOONEP_NEED(topk_idx);

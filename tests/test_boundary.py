@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 19, names
+    assert len(names) == 20, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -190,6 +190,18 @@ int main(void) {
   if (moonep_plan_workspace_bytes(&d, &bytes) != MOONEP_ERR_SLOTS) return 4;
   if (moonep_plan_workspace_bytes(NULL, &bytes) != MOONEP_ERR_ARG) return 5;
   if (strlen(moonep_status_string(MOONEP_ERR_ROUTING)) == 0) return 6;
+  {
+    /* views are host arithmetic on the layout: no GPU work, any aligned base */
+    moonep_plan_view v;
+    const char* base = (const char*)0 + 4096;
+    d.B = 48;
+    if (moonep_plan_views(&d, base, &v) != MOONEP_OK) return 7;
+    if ((const char*)v.cu_seqlens != base + lay.cu_seqlens || (const char*)v.dst != base + lay.dst ||
+        (const char*)v.inverse != base + lay.inverse || (const char*)v.slot_expert != base + lay.slot_expert ||
+        (const char*)v.status != base + lay.status) return 8;
+    if (moonep_plan_views(&d, base + 8, &v) != MOONEP_ERR_ALIGN) return 9;
+    if (moonep_plan_views(&d, NULL, &v) != MOONEP_ERR_ARG) return 10;
+  }
   printf("%zu\n", total);
   return 0;
 }
@@ -224,7 +236,8 @@ def test_binding_structs_match_the_header(tmp_path):
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
-    structs = {"moonep_dims": _lib.moonep_dims, "moonep_plan_layout": _lib.moonep_plan_layout}
+    structs = {"moonep_dims": _lib.moonep_dims, "moonep_plan_layout": _lib.moonep_plan_layout,
+               "moonep_plan_view": _lib.moonep_plan_view}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moonep.h"', 'int main(void) {']
     for sname, cls in structs.items():
         lines.append(f'  printf("{sname} sizeof %zu\\n", sizeof({sname}));')
@@ -248,3 +261,17 @@ def test_binding_structs_match_the_header(tmp_path):
     body = re.search(r"typedef struct moonep_plan_layout \{(.*?)\}", text, flags=re.S).group(1)
     declared = re.findall(r"\b(\w+)\s*;", body)
     assert declared == [f for f, _ in _lib.moonep_plan_layout._fields_]
+
+
+def test_plan_views_point_at_the_layout_tables(lib):
+    # host-only: the view of a workspace at any aligned device address is that
+    # address plus the layout's offsets
+    d = mx.dims(8, 64, 8, 4, 1024, 1024, 512)
+    lay = mx.moonep_get_plan_layout(d)
+    base = 1 << 30
+    v = mx.moonep_plan_views(d, base)
+    assert v == {"cu_seqlens": base + lay.cu_seqlens, "dst": base + lay.dst,
+                 "inverse": base + lay.inverse, "slot_expert": base + lay.slot_expert,
+                 "status": base + lay.status}
+    with pytest.raises(mx.MoonepError):
+        mx.moonep_plan_views(d, base + 4)
